@@ -1,0 +1,187 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 (sm_103a) speculative-decoding verify step.
+ *
+ * What the call computes.  A target model has scored a block of drafted
+ * tokens in one forward pass; this library turns the target logits and the
+ * draft logits into the tokens that are kept.  The rules come from the
+ * source pages:
+ *   - draft -> verify -> accept/reject: accept drafted tokens from the first
+ *     one while the check passes, resample one token at the first failure,
+ *     drop every later candidate, and emit one extra target token when the
+ *     whole block passes ("DeepSeek DSpark speculative decoding" tutorial,
+ *     section "推测解码的两步流程"; the DSpine page, section "原理");
+ *   - the check is lossless rejection sampling (DFlash/Spec V2 page, A3, and
+ *     its citation of Leviathan et al.; DSpark tutorial, FAQ):
+ *     accept x_j iff u_j * p_d(x_j) < p_t(x_j); the replacement is drawn from
+ *     max(0, p_t - p_d) renormalised; the bonus token from p_t;
+ *   - greedy decoding accepts x_j iff it equals the target argmax (DFlash
+ *     page, A4: greedy evaluations);
+ *   - confidence label c*_j = 1 - 1/2 * ||p_d,j - p_t,j||_1 for every drafted
+ *     position (DSpark tutorial, section "置信度预测头");
+ *   - ragged per-request verify length l_r (DSpark tutorial, section
+ *     "硬件感知前缀调度器"); block 16 = 1 start token + 15 guesses (DSpine
+ *     page, section "这份权重是什么");
+ *   - temperature, top_k, top_p processing of both models (DSpine page,
+ *     section "加速效果": T 1.0, top_p 0.95, top_k 20).
+ * Readings the pages leave open (filter order temperature -> top-k ->
+ * renormalise -> top-p -> renormalise; ties broken by (value desc, id asc);
+ * inverse CDF over ascending ids with a strict ">"; one uniform per target
+ * row) are the same as the CPU oracle's and are listed in the design doc.
+ *
+ * Layout.  B requests; request r owns l_r target rows (1 <= l_r <= max_len):
+ * rows row_offsets[r] .. row_offsets[r] + l_r - 1 of target_logits, where
+ * target row j < l_r - 1 scores drafted token j and row l_r - 1 is the bonus
+ * row.  Request r owns l_r - 1 draft rows starting at row row_offsets[r] - r
+ * of draft_logits.  N_t = row_offsets[B] = sum l_r, N_d = N_t - B.  All
+ * logits are row-major with row stride V elements.
+ *
+ * Ownership and memory.  The caller owns every buffer.  The library
+ * allocates nothing: scratch lives in the caller's workspace (size from
+ * spec_verify_workspace_size).  Device pointers must be device memory of
+ * the current CUDA device.  The logits base pointers must be 16-byte
+ * aligned; other device pointers 4-byte aligned; the workspace 256-byte
+ * aligned.
+ *
+ * Streams.  Every call only enqueues work on `stream` (a cudaStream_t; NULL
+ * is the legacy default stream) and returns without synchronising the host.
+ * Host-visible argument errors are returned before anything is enqueued.
+ * Data-dependent problems are OR-ed into *dev_error on the device (never a
+ * trap); outputs of a request whose data raised a flag are unspecified.
+ * The caller zeroes *dev_error before the call if it wants this call's
+ * flags only.  Calls that share a workspace must be ordered on the GPU.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype of both logits buffers */
+#define SV_BF16 0 /* bfloat16, 2 bytes */
+#define SV_FP32 1 /* float32, 4 bytes */
+
+/* verify mode */
+#define SV_GREEDY 0
+#define SV_SAMPLE 1
+
+/* host status codes (return values) */
+#define SV_OK 0
+#define SV_ERR_ARG (-1)         /* null/misaligned pointer, bad size or parameter */
+#define SV_ERR_DTYPE (-2)       /* dtype is neither SV_BF16 nor SV_FP32 */
+#define SV_ERR_CUDA (-3)        /* a CUDA runtime call or a launch failed */
+#define SV_ERR_UNSUPPORTED (-4) /* filter combination or cluster shape not available */
+#define SV_ERR_WORKSPACE (-5)   /* workspace missing, misaligned or too small */
+
+/* device error bits OR-ed into *dev_error */
+#define SV_DEVERR_NAN 1     /* a row holds NaN or +inf, or is entirely -inf */
+#define SV_DEVERR_TOKEN 2   /* a drafted token is outside [0, V) */
+#define SV_DEVERR_LEN 4     /* l_r outside [1, max_len] or row_offsets inconsistent */
+#define SV_DEVERR_TIMEOUT 8 /* a bounded device wait gave up */
+
+/* limits */
+#define SV_MAX_LEN 256       /* largest accepted max_len */
+#define SV_MAX_FILTER_K 64   /* largest top_k served together with top_p < 1 */
+
+/*
+ * Bytes of workspace a call with these sizes needs (a multiple of 256).
+ * Pure host function; touches no device.
+ */
+size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows);
+
+/*
+ * The verify step: spec_verify_rows followed by spec_verify_finalize on the
+ * same stream.
+ *
+ *  target_logits  [N_t, V] device, dtype; 16-byte aligned base.
+ *  draft_logits   [N_d, V] device, dtype; may be NULL when N_d == 0.
+ *  draft_tokens   [N_d] int32 device: drafted token of each draft row.
+ *  uniforms       [N_t] float32 device, values in [0, 1): u of target row
+ *                 off_r + j tests drafted token j (j < l_r - 1); the one of
+ *                 row off_r + l_r - 1 drives the replacement / bonus draw.
+ *  verify_lens    [B] int32 device: l_r.
+ *  row_offsets    [B+1] int32 device: prefix sums of l_r, row_offsets[0] = 0.
+ *  B, V           > 0.
+ *  n_target_rows  N_t on the host (must equal row_offsets[B]; checked on
+ *                 the device, SV_DEVERR_LEN).
+ *  max_len        host upper bound of every l_r, 1..SV_MAX_LEN.
+ *  dtype          SV_BF16 or SV_FP32.
+ *  temperature    T > 0 (required in sampling mode and whenever out_conf or
+ *                 out_row_stats is requested; otherwise ignored).
+ *  top_k          <= 0 or >= V: off.  Else keep the top_k tokens.
+ *  top_p          in (0, 1]; 1 = off.  top_p < 1 needs 1 <= top_k <=
+ *                 SV_MAX_FILTER_K (full-vocabulary top-p is not served:
+ *                 SV_ERR_UNSUPPORTED); top_k in (SV_MAX_FILTER_K, V) is
+ *                 likewise not served yet.
+ *  mode           SV_GREEDY or SV_SAMPLE.
+ *  out_tokens     [N_t] int32 device: for request r, entries off_r .. off_r
+ *                 + a_r - 1 = accepted drafts, entry off_r + a_r = the final
+ *                 (replacement, bonus or greedy) token, later entries -1.
+ *  out_accept_len [B] int32 device: a_r in [0, l_r - 1].
+ *  out_conf       [N_d] float32 device or NULL: c* per draft row.
+ *  out_row_stats  [N_t + N_d][3] float32 device or NULL: per row (target
+ *                 rows first, then draft rows) m = max logit / T, Z = sum
+ *                 over the kept set of exp(logit / T - m), argmax (lowest
+ *                 id; the int32 bit pattern stored in the float slot).
+ *  dev_error      [1] int32 device or NULL: device error bits (see above).
+ *  workspace      device scratch of workspace_bytes >= spec_verify_workspace_size.
+ *  stream         cudaStream_t.
+ * Returns SV_OK or a negative SV_ERR_* code.
+ */
+int spec_verify(const void* target_logits, const void* draft_logits,
+                const int32_t* draft_tokens, const float* uniforms,
+                const int32_t* verify_lens, const int32_t* row_offsets,
+                int32_t B, int32_t V, int32_t n_target_rows, int32_t max_len,
+                int32_t dtype, float temperature, int32_t top_k, float top_p, int32_t mode,
+                int32_t* out_tokens, int32_t* out_accept_len, float* out_conf,
+                float* out_row_stats, int32_t* dev_error,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Phase 1 of spec_verify (same arguments; out_tokens and out_accept_len are
+ * not touched).  One thread-block cluster per target row streams the target
+ * row and its draft partner from HBM into the cluster's shared memory once,
+ * and writes the per-row statistics, c* labels and per-position accept
+ * decisions (into the workspace, and into out_conf / out_row_stats when
+ * given).  This is the bandwidth-bound kernel.
+ */
+int spec_verify_rows(const void* target_logits, const void* draft_logits,
+                     const int32_t* draft_tokens, const float* uniforms,
+                     const int32_t* verify_lens, const int32_t* row_offsets,
+                     int32_t B, int32_t V, int32_t n_target_rows, int32_t max_len,
+                     int32_t dtype, float temperature, int32_t top_k, float top_p, int32_t mode,
+                     int32_t* out_tokens, int32_t* out_accept_len, float* out_conf,
+                     float* out_row_stats, int32_t* dev_error,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Phase 2 of spec_verify (same arguments).  Per request: the first-rejection
+ * scan over the accept decisions left in the workspace by phase 1, then the
+ * final token -- in unfiltered sampling mode an inverse-CDF draw over the one
+ * rejected row pair (or the bonus row) re-read from HBM -- and the outputs.
+ * Must run after spec_verify_rows with identical arguments and workspace.
+ */
+int spec_verify_finalize(const void* target_logits, const void* draft_logits,
+                         const int32_t* draft_tokens, const float* uniforms,
+                         const int32_t* verify_lens, const int32_t* row_offsets,
+                         int32_t B, int32_t V, int32_t n_target_rows, int32_t max_len,
+                         int32_t dtype, float temperature, int32_t top_k, float top_p,
+                         int32_t mode, int32_t* out_tokens, int32_t* out_accept_len,
+                         float* out_conf, float* out_row_stats, int32_t* dev_error,
+                         void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static text for a status code (host). */
+const char* spec_verify_status_string(int status);
+
+/* Cluster size (CTAs per target row) the rows kernel would use for V and
+ * dtype on the current device, or a negative SV_ERR_* code. */
+int spec_verify_cluster_size(int32_t V, int32_t dtype, int32_t top_k, float top_p);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -1,0 +1,175 @@
+"""ctypes binding of libspecverify.so (the C ABI in include/spec_verify.h).
+
+Argument marshalling only: every step of the verify path runs in the
+library's kernels.  torch is used for device memory (outputs, workspace)
+and for the current CUDA stream.  Importing this module fails loudly when
+the library has not been built -- there is no fallback path.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libspecverify.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it first (python -m "
+        "speculative_decoding_verification_16_gb300.build, or __graft_entry__.build())")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+SV_BF16, SV_FP32 = 0, 1
+SV_GREEDY, SV_SAMPLE = 0, 1
+SV_OK = 0
+SV_DEVERR_NAN, SV_DEVERR_TOKEN, SV_DEVERR_LEN, SV_DEVERR_TIMEOUT = 1, 2, 4, 8
+
+_vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
+_ARGTYPES = [_vp, _vp, _vp, _vp, _vp, _vp,            # logits, tokens, uniforms, lens, offsets
+             _i32, _i32, _i32, _i32,                  # B, V, n_target_rows, max_len
+             _i32, _f32, _i32, _f32, _i32,            # dtype, T, top_k, top_p, mode
+             _vp, _vp, _vp, _vp, _vp,                 # outputs, dev_error
+             _vp, _sz, _vp]                           # workspace, bytes, stream
+for _name in ("spec_verify", "spec_verify_rows", "spec_verify_finalize"):
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _ARGTYPES
+    _fn.restype = ctypes.c_int
+_lib.spec_verify_workspace_size.argtypes = [_i32, _i32]
+_lib.spec_verify_workspace_size.restype = ctypes.c_size_t
+_lib.spec_verify_status_string.argtypes = [ctypes.c_int]
+_lib.spec_verify_status_string.restype = ctypes.c_char_p
+_lib.spec_verify_cluster_size.argtypes = [_i32, _i32, _i32, _f32]
+_lib.spec_verify_cluster_size.restype = ctypes.c_int
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int):
+        super().__init__(f"spec_verify failed ({status}): {spec_verify_status_string(status)}")
+        self.status = status
+
+
+def spec_verify_status_string(status: int) -> str:
+    return _lib.spec_verify_status_string(int(status)).decode()
+
+
+def spec_verify_workspace_size(B: int, n_target_rows: int) -> int:
+    return int(_lib.spec_verify_workspace_size(int(B), int(n_target_rows)))
+
+
+def spec_verify_cluster_size(V: int, dtype: int, top_k: int = 0, top_p: float = 1.0) -> int:
+    return int(_lib.spec_verify_cluster_size(int(V), int(dtype), int(top_k), float(top_p)))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    if t.dtype == torch.float32:
+        return SV_FP32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+class Outputs:
+    """Device output buffers of one call."""
+
+    def __init__(self, tokens, accept_len, conf, row_stats, dev_error):
+        self.tokens = tokens
+        self.accept_len = accept_len
+        self.conf = conf
+        self.row_stats = row_stats
+        self.dev_error = dev_error
+
+
+def alloc_outputs(n_target_rows: int, B: int, device, want_conf=True, want_stats=False):
+    Nd = n_target_rows - B
+    return Outputs(
+        torch.empty(n_target_rows, dtype=torch.int32, device=device),
+        torch.empty(B, dtype=torch.int32, device=device),
+        torch.empty(Nd, dtype=torch.float32, device=device) if want_conf else None,
+        torch.empty((n_target_rows + Nd, 3), dtype=torch.float32, device=device)
+        if want_stats else None,
+        torch.zeros(1, dtype=torch.int32, device=device))
+
+
+def alloc_workspace(B: int, n_target_rows: int, device) -> torch.Tensor:
+    return torch.empty(spec_verify_workspace_size(B, n_target_rows), dtype=torch.uint8,
+                       device=device)
+
+
+class PreparedCall:
+    """A call with its arguments marshalled once; ``__call__`` re-issues it
+    (used by timing loops, where per-call marshalling would dominate)."""
+
+    def __init__(self, fn, args):
+        self._fn = fn
+        self._args = args
+
+    def __call__(self):
+        rc = self._fn(*self._args)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc)
+
+
+def prepare(entry: str, target_logits, draft_logits, draft_tokens, uniforms, verify_lens,
+            row_offsets, *, max_len, temperature=1.0, top_k=0, top_p=1.0, mode=SV_SAMPLE,
+            out: Outputs, workspace: torch.Tensor, stream=None) -> PreparedCall:
+    """Marshal the arguments of one C entry point (``spec_verify``,
+    ``spec_verify_rows`` or ``spec_verify_finalize``)."""
+    B = verify_lens.numel()
+    n_target_rows, V = target_logits.shape
+    if stream is None:
+        stream = torch.cuda.current_stream(target_logits.device)
+    args = (_ptr(target_logits), _ptr(draft_logits) if draft_logits.numel() else None,
+            _ptr(draft_tokens) if draft_tokens.numel() else None, _ptr(uniforms),
+            _ptr(verify_lens), _ptr(row_offsets),
+            _i32(B), _i32(V), _i32(n_target_rows), _i32(max_len),
+            _i32(_dtype_code(target_logits)), _f32(temperature), _i32(top_k), _f32(top_p),
+            _i32(mode),
+            _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.conf), _ptr(out.row_stats),
+            _ptr(out.dev_error), _ptr(workspace), _sz(workspace.numel()),
+            ctypes.c_void_p(stream.cuda_stream))
+    return PreparedCall(getattr(_lib, entry), args)
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, uniforms, verify_lens, row_offsets,
+                *, max_len=16, temperature=1.0, top_k=0, top_p=1.0, mode=SV_SAMPLE,
+                want_conf=True, want_stats=False, out: Outputs | None = None,
+                workspace: torch.Tensor | None = None, stream=None) -> Outputs:
+    """One verify call on the current (or given) stream; returns device
+    outputs without synchronising.  Tensors must be contiguous CUDA tensors:
+    logits bf16/fp32 [N_t, V] and [N_d, V], int32 tokens/lengths/offsets,
+    float32 uniforms."""
+    for t in (target_logits, draft_logits, draft_tokens, uniforms, verify_lens, row_offsets):
+        if not t.is_contiguous():
+            raise ValueError("inputs must be contiguous")
+    B = verify_lens.numel()
+    n_target_rows = target_logits.shape[0]
+    dev = target_logits.device
+    if out is None:
+        out = alloc_outputs(n_target_rows, B, dev, want_conf, want_stats)
+    else:
+        out.dev_error.zero_()
+    if workspace is None:
+        workspace = alloc_workspace(B, n_target_rows, dev)
+    prepare("spec_verify", target_logits, draft_logits, draft_tokens, uniforms, verify_lens,
+            row_offsets, max_len=max_len, temperature=temperature, top_k=top_k, top_p=top_p,
+            mode=mode, out=out, workspace=workspace, stream=stream)()
+    return out
+
+
+def verify_workload(w, *, want_conf=True, want_stats=False, **kw) -> Outputs:
+    """Run the library on a ``workloads.Workload`` held on a CUDA device."""
+    spec = w.spec
+    return spec_verify(w.target, w.draft, w.draft_tokens, w.uniforms, w.verify_lens,
+                       w.row_offsets, max_len=kw.pop("max_len", spec.max_len),
+                       temperature=kw.pop("temperature", spec.temperature),
+                       top_k=kw.pop("top_k", spec.top_k), top_p=kw.pop("top_p", spec.top_p),
+                       mode=kw.pop("mode", w.mode), want_conf=want_conf, want_stats=want_stats,
+                       **kw)

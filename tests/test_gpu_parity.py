@@ -1,0 +1,236 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs, element by element, under the stated tolerance rules."""
+
+import json
+import os
+from contextlib import contextmanager
+
+import numpy as np
+import pytest
+import torch
+
+from parity_helpers import compare, oracle_requests
+from speculative_decoding_verification_16_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@contextmanager
+def cluster_size(c):
+    old = os.environ.get("SPEC_VERIFY_CLUSTER")
+    if c is None:
+        os.environ.pop("SPEC_VERIFY_CLUSTER", None)
+    else:
+        os.environ["SPEC_VERIFY_CLUSTER"] = str(c)
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("SPEC_VERIFY_CLUSTER", None)
+        else:
+            os.environ["SPEC_VERIFY_CLUSTER"] = old
+
+
+def run_and_compare(cuda_lib, w, *, requests=None, T=None, top_k=None, top_p=None,
+                    want_conf=True, want_stats=True, mode=None, min_checked=1):
+    spec = w.spec
+    T = spec.temperature if T is None else T
+    top_k = spec.top_k if top_k is None else top_k
+    top_p = spec.top_p if top_p is None else top_p
+    mode = w.mode if mode is None else mode
+    out = cuda_lib.verify_workload(w, want_conf=want_conf, want_stats=want_stats,
+                                   temperature=T, top_k=top_k, top_p=top_p, mode=mode)
+    torch.cuda.synchronize()
+    assert int(out.dev_error.item()) == 0
+    requests = range(w.B) if requests is None else requests
+    ref = oracle_requests(w, requests, mode=mode, temperature=T, top_k=top_k, top_p=top_p,
+                          want_conf=want_conf or want_stats)
+    n, n_tie = compare(w, out, ref, check_stats=want_stats, check_conf=want_conf)
+    assert n - n_tie >= min_checked
+    return out, ref
+
+
+SMALL = [
+    # (workload index, V, B, lens, forced cluster)
+    (0, None, None, None, None),
+    (1, 20000, None, None, 1),
+    (1, 20000, None, None, 4),
+    (1, 20000, None, None, 16),
+    (2, 8191, 6, None, 8),          # odd V: rows not 16-byte aligned
+    (2, 4099, 5, None, 3),          # cluster size that is not a power of two
+    (3, 5003, 40, None, 4),         # ragged lengths
+    (3, 777, None, [1, 16, 2, 1, 9], 2),
+]
+
+
+@pytest.mark.parametrize("mode", [W.SAMPLE, W.GREEDY])
+@pytest.mark.parametrize("idx,V,B,lens,C", SMALL)
+def test_small_workloads_every_request(cuda_lib, idx, V, B, lens, C, mode):
+    w = W.make_workload(W.WORKLOADS[idx], mode, seed=7 + idx, device=DEV, B=B, V=V, lens=lens)
+    with cluster_size(C):
+        run_and_compare(cuda_lib, w)
+
+
+@pytest.mark.parametrize("idx,mode,sample", [
+    (1, W.SAMPLE, None), (1, W.GREEDY, None),
+    (2, W.SAMPLE, None), (2, W.GREEDY, None),
+    (3, W.SAMPLE, 40),
+])
+def test_full_size_workloads(cuda_lib, idx, mode, sample):
+    """Full sizes in the launch configuration the bench times; the oracle
+    checks every request (or a seeded sample of them)."""
+    spec = W.WORKLOADS[idx]
+    w = W.make_workload(spec, mode, seed=idx, device=DEV)
+    reqs = None
+    if sample is not None:
+        reqs = sorted(np.random.default_rng(idx).choice(w.B, size=sample, replace=False).tolist())
+    run_and_compare(cuda_lib, w, requests=reqs, want_stats=True)
+
+
+def _pair_workload(t, d, x, lens, u, spec=W.WORKLOADS[2], mode=W.SAMPLE):
+    lens_t = torch.tensor(lens, dtype=torch.int32, device=DEV)
+    offs = torch.zeros(len(lens) + 1, dtype=torch.int32, device=DEV)
+    offs[1:] = torch.cumsum(lens_t, 0)
+    return W.Workload(spec, mode, t.contiguous(), d.contiguous(),
+                      x.to(torch.int32).contiguous(), u.to(torch.float32).contiguous(), lens_t,
+                      offs)
+
+
+def test_no_drafted_positions(cuda_lib):
+    w0 = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=3, device=DEV, V=3000, lens=[1] * 7)
+    assert w0.draft.shape[0] == 0
+    out, _ = run_and_compare(cuda_lib, w0)
+    assert (out.accept_len.cpu() == 0).all()
+
+
+def test_identical_rows_accept_all(cuda_lib):
+    base = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=4, device=DEV, B=6, V=30011)
+    offs = base.row_offsets.cpu().numpy()
+    d = torch.cat([base.target[offs[r]:offs[r + 1] - 1] for r in range(base.B)])
+    # drafted tokens drawn from the (shared) distribution
+    g = torch.Generator(device=DEV).manual_seed(1)
+    x = torch.multinomial(torch.softmax(d.float(), 1), 1, generator=g).flatten()
+    w = _pair_workload(base.target, d, x, [16] * 6, base.uniforms)
+    out, _ = run_and_compare(cuda_lib, w, min_checked=0)
+    assert (out.accept_len.cpu() == 15).all()
+    assert np.allclose(out.conf.cpu().numpy(), 1.0, atol=1e-5)
+
+
+def test_disjoint_supports(cuda_lib):
+    base = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=5, device=DEV, B=4, V=4096)
+    t = base.target.clone()
+    d = base.draft.clone()
+    t[:, 1::2] = float("-inf")
+    d[:, 0::2] = float("-inf")
+    g = torch.Generator(device=DEV).manual_seed(2)
+    x = torch.multinomial(torch.softmax(d.float(), 1), 1, generator=g).flatten()
+    w = _pair_workload(t, d, x, [16] * 4, base.uniforms)
+    out, _ = run_and_compare(cuda_lib, w)
+    assert (out.accept_len.cpu() == 0).all()
+    assert np.allclose(out.conf.cpu().numpy(), 0.0, atol=1e-6)
+    offs = w.row_offsets.cpu().numpy()
+    assert all(int(out.tokens[offs[r]]) % 2 == 0 for r in range(4))
+
+
+def test_tied_maxima_lowest_id(cuda_lib):
+    V = 9000
+    t = torch.zeros((6, V), dtype=torch.bfloat16, device=DEV)
+    for i, ids in enumerate([[5, 7000], [8999, 3], [100, 101, 102], [0, 8998], [4500], [1, 8000]]):
+        t[i, ids] = 2.0
+    d = t[:5].clone()
+    x = torch.tensor([5, 3, 101, 0, 4500], device=DEV)
+    w = _pair_workload(t, d, x, [6], torch.full((6,), 0.5, device=DEV), mode=W.GREEDY)
+    out, _ = run_and_compare(cuda_lib, w)
+    stats = out.row_stats.cpu().numpy()[:6, 2].view(np.int32)
+    assert stats.tolist() == [5, 3, 100, 0, 4500, 1]
+    assert int(out.accept_len[0]) == 2  # x0 = 5 ok, x1 = 3 ok, x2 = 101 != 100
+
+
+@pytest.mark.parametrize("T", [0.05, 0.7, 10.0])
+def test_temperatures(cuda_lib, T):
+    w = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=9, device=DEV, B=6, V=12000)
+    run_and_compare(cuda_lib, w, T=T)
+
+
+def test_greedy_without_labels_or_stats(cuda_lib):
+    w = W.make_workload(W.WORKLOADS[2], W.GREEDY, seed=10, device=DEV, B=8, V=50000)
+    run_and_compare(cuda_lib, w, want_conf=False, want_stats=False)
+
+
+def test_hand_derived_cases_on_gpu(cuda_lib):
+    path = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
+    for case in json.load(open(path))["cases"]:
+        if case["top_k"] or case["top_p"] < 1:
+            continue  # filtered cases are covered by the filtered-kernel tests
+        rows = lambda rs: torch.tensor([[float(v) for v in r] for r in rs],  # noqa: E731
+                                       dtype=torch.float32, device=DEV)
+        t = rows(case["target"])
+        d = rows(case["draft"]) if case["draft"] else torch.zeros((0, t.shape[1]), device=DEV)
+        mode = W.SAMPLE if case["mode"] == "sample" else W.GREEDY
+        w = _pair_workload(t, d, torch.tensor(case["draft_tokens"], device=DEV),
+                           case["verify_lens"], torch.tensor(case["uniforms"], device=DEV),
+                           mode=mode)
+        out = cuda_lib.verify_workload(w, temperature=case["temperature"], top_k=0, top_p=1.0,
+                                       max_len=16)
+        torch.cuda.synchronize()
+        assert out.tokens.cpu().tolist() == case["tokens"], case["name"]
+        assert out.accept_len.cpu().tolist() == case["accept_len_expected"], case["name"]
+        np.testing.assert_allclose(out.conf.cpu().numpy(), case["conf"], atol=1e-6,
+                                   err_msg=case["name"])
+
+
+def test_device_error_flags(cuda_lib):
+    base = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=12, device=DEV, B=3, V=2048)
+    t = base.target.clone()
+    t[3, 17] = float("nan")
+    w = _pair_workload(t, base.draft, base.draft_tokens, [16] * 3, base.uniforms)
+    out = cuda_lib.verify_workload(w)
+    torch.cuda.synchronize()
+    assert int(out.dev_error.item()) & cuda_lib.SV_DEVERR_NAN
+    x = base.draft_tokens.clone()
+    x[4] = 2048
+    w = _pair_workload(base.target, base.draft, x, [16] * 3, base.uniforms)
+    out = cuda_lib.verify_workload(w)
+    torch.cuda.synchronize()
+    assert int(out.dev_error.item()) & cuda_lib.SV_DEVERR_TOKEN
+    w = _pair_workload(base.target, base.draft, base.draft_tokens, [16] * 3, base.uniforms)
+    w.verify_lens[1] = 15  # offsets no longer match the lengths
+    out = cuda_lib.verify_workload(w)
+    torch.cuda.synchronize()
+    assert int(out.dev_error.item()) & cuda_lib.SV_DEVERR_LEN
+    t = base.target.clone()
+    t[0, :] = float("-inf")
+    w = _pair_workload(t, base.draft, base.draft_tokens, [16] * 3, base.uniforms)
+    out = cuda_lib.verify_workload(w)
+    torch.cuda.synchronize()
+    assert int(out.dev_error.item()) & cuda_lib.SV_DEVERR_NAN
+
+
+def test_host_errors_through_binding(cuda_lib):
+    w = W.make_workload(W.WORKLOADS[0], W.SAMPLE, seed=0, device=DEV)
+    with pytest.raises(cuda_lib.SpecVerifyError):
+        cuda_lib.verify_workload(w, temperature=0.0)
+    with pytest.raises(cuda_lib.SpecVerifyError):
+        cuda_lib.verify_workload(w, max_len=0)
+
+
+def test_deterministic_across_runs_and_cluster_sizes(cuda_lib):
+    w = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=13, device=DEV, B=8, V=40000)
+    first = None
+    for C in (None, None, 1, 2, 4, 8, 16):
+        with cluster_size(C):
+            out = cuda_lib.verify_workload(w, want_stats=True)
+        torch.cuda.synchronize()
+        cur = (out.tokens.cpu().numpy(), out.accept_len.cpu().numpy(), out.conf.cpu().numpy(),
+               out.row_stats.cpu().numpy())
+        if first is None:
+            first = cur
+            continue
+        if C is None:  # same configuration: bitwise identical
+            for a, b in zip(first, cur):
+                assert np.array_equal(a, b)
+        else:
+            np.testing.assert_allclose(cur[2], first[2], atol=2e-6)
+            np.testing.assert_allclose(cur[3][:, :2], first[3][:, :2], rtol=2e-6)
