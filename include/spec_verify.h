@@ -176,9 +176,10 @@ int spec_verify_finalize(const void* target_logits, const void* draft_logits,
 /* Static text for a status code (host). */
 const char* spec_verify_status_string(int status);
 
-/* Cluster size (CTAs per target row) the rows kernel would use for V and
- * dtype on the current device, or a negative SV_ERR_* code. */
-int spec_verify_cluster_size(int32_t V, int32_t dtype, int32_t top_k, float top_p);
+/* Number of vocabulary slices (work units, each held by one CTA) into which
+ * the rows kernel cuts a row of V logits of this dtype on the current
+ * device, or a negative SV_ERR_* code. */
+int spec_verify_slices_per_row(int32_t V, int32_t dtype, int32_t top_k, float top_p);
 
 #ifdef __cplusplus
 }

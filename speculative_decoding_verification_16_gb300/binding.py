@@ -42,8 +42,8 @@ _lib.spec_verify_workspace_size.argtypes = [_i32, _i32]
 _lib.spec_verify_workspace_size.restype = ctypes.c_size_t
 _lib.spec_verify_status_string.argtypes = [ctypes.c_int]
 _lib.spec_verify_status_string.restype = ctypes.c_char_p
-_lib.spec_verify_cluster_size.argtypes = [_i32, _i32, _i32, _f32]
-_lib.spec_verify_cluster_size.restype = ctypes.c_int
+_lib.spec_verify_slices_per_row.argtypes = [_i32, _i32, _i32, _f32]
+_lib.spec_verify_slices_per_row.restype = ctypes.c_int
 
 
 class SpecVerifyError(RuntimeError):
@@ -60,8 +60,8 @@ def spec_verify_workspace_size(B: int, n_target_rows: int) -> int:
     return int(_lib.spec_verify_workspace_size(int(B), int(n_target_rows)))
 
 
-def spec_verify_cluster_size(V: int, dtype: int, top_k: int = 0, top_p: float = 1.0) -> int:
-    return int(_lib.spec_verify_cluster_size(int(V), int(dtype), int(top_k), float(top_p)))
+def spec_verify_slices_per_row(V: int, dtype: int, top_k: int = 0, top_p: float = 1.0) -> int:
+    return int(_lib.spec_verify_slices_per_row(int(V), int(dtype), int(top_k), float(top_p)))
 
 
 def _ptr(t):
@@ -99,7 +99,9 @@ def alloc_outputs(n_target_rows: int, B: int, device, want_conf=True, want_stats
 
 
 def alloc_workspace(B: int, n_target_rows: int, device) -> torch.Tensor:
-    return torch.empty(spec_verify_workspace_size(B, n_target_rows), dtype=torch.uint8,
+    """Device workspace for calls with these sizes, zeroed as the C ABI
+    requires before its first use."""
+    return torch.zeros(spec_verify_workspace_size(B, n_target_rows), dtype=torch.uint8,
                        device=device)
 
 

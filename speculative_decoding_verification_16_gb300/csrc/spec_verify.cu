@@ -9,6 +9,8 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "spec_verify.h"
@@ -62,28 +64,30 @@ bool is_filtered(int V, int top_k, float top_p) {
   return (top_k > 0 && top_k < V) || top_p < 1.0f;
 }
 
-// Cluster size of the rows kernel: the smallest C in {1, 2, 4, 8, 16} whose
-// slice pair fits the shared-memory budget (SPEC_VERIFY_SMEM_BUDGET bytes,
-// default 80 KiB: two CTAs per SM); SPEC_VERIFY_CLUSTER forces a size.
-int rows_cluster(int V, int es, const DeviceCache& dc, int* smem_out) {
-  const int forced = env_int("SPEC_VERIFY_CLUSTER", 0);
-  const int budget = env_int("SPEC_VERIFY_SMEM_BUDGET", 80 * 1024);
-  if (forced > 0) {
-    if (forced > kMaxCluster) return SV_ERR_UNSUPPORTED;
-    const int smem = kHdrBytes + 2 * rowbuf_bytes(slice_len(V, forced, es), es);
-    if (smem > dc.max_smem_optin) return SV_ERR_UNSUPPORTED;
-    *smem_out = smem;
-    return forced;
-  }
-  for (int C = 1; C <= kMaxCluster; C *= 2) {
-    const int smem = kHdrBytes + 2 * rowbuf_bytes(slice_len(V, C, es), es);
-    if (smem > dc.max_smem_optin) continue;
-    if (smem <= budget || C == kMaxCluster) {
-      *smem_out = smem;
-      return C;
+// Geometry of the rows kernel: a row is cut into S <= kMaxSlices slices of
+// L elements (L a multiple of the 16-byte vector, about 8192 bf16 / 4096
+// fp32 elements by default: SPEC_VERIFY_SLICE overrides); as many stages
+// (kDelay + 2 .. kMaxStages) as the shared memory allows.
+struct RowsGeom {
+  int L, S, stages, smem;
+};
+
+int rows_geometry(int V, int es, const DeviceCache& dc, RowsGeom* g) {
+  const int vec = 16 / es;
+  const int target = env_int("SPEC_VERIFY_SLICE", 16384 / es);
+  int S = std::max(1, (V + target - 1) / target);
+  S = std::min(S, kMaxSlices);
+  int L = round_up((V + S - 1) / S, vec);
+  S = (V + L - 1) / L;  // no empty trailing slice
+  const int max_stages = std::min(kMaxStages, env_int("SPEC_VERIFY_STAGES", kMaxStages));
+  for (int ns = max_stages; ns >= kDelay + 2; --ns) {
+    const int smem = kRowsHdrBytes + ns * 2 * rowbuf_bytes(L, es);
+    if (smem + kMaxSmemOffsets * 4 <= dc.max_smem_optin) {
+      *g = RowsGeom{L, S, ns, smem};
+      return SV_OK;
     }
   }
-  return SV_ERR_UNSUPPORTED;
+  return SV_ERR_UNSUPPORTED;  // rows too long for kMaxSlices slices in shared memory
 }
 
 // Cluster size of the unfiltered final draw (one request per cluster).
@@ -101,20 +105,57 @@ int draw_cluster(int V, int es, const DeviceCache& dc, int* smem_out) {
   return SV_ERR_UNSUPPORTED;
 }
 
+// The dynamic shared-memory limit is raised to the device maximum (not to
+// this launch's size), so that one setting serves every configuration.
 template <typename K>
-cudaError_t prepare_kernel(K kernel, int smem, int cluster) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+cudaError_t prepare_kernel(K kernel, int max_smem, int cluster) {
+  cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
   if (e == cudaSuccess && cluster > 8)
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   return e;
 }
 
+// Kernel attributes and the cluster-occupancy check are host calls that can
+// cost microseconds; they run once per (device, kernel, smem, cluster size).
+struct PreparedKey {
+  int dev;
+  const void* fn;
+  int smem;
+  int cluster;
+  int status;
+};
+constexpr int kMaxPrepared = 256;
+PreparedKey g_prepared[kMaxPrepared];
+int g_nprepared = 0;
+
+int find_prepared(int dev, const void* fn, int smem, int C) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < g_nprepared; ++i) {
+    const PreparedKey& k = g_prepared[i];
+    if (k.dev == dev && k.fn == fn && k.smem == smem && k.cluster == C) return k.status;
+  }
+  return -1000;  // not prepared yet
+}
+
+void remember_prepared(int dev, const void* fn, int smem, int C, int status) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_nprepared < kMaxPrepared) g_prepared[g_nprepared++] = PreparedKey{dev, fn, smem, C, status};
+}
+
+// Launch `kernel` with clusters of C CTAs of `threads` threads.  nclusters
+// > 0: that many clusters; nclusters < 0: one persistent wave of
+// min(-nclusters, resident clusters) clusters.
 template <typename K>
-int launch_cluster(K kernel, const Params& P, int nclusters, int C, int smem, cudaStream_t stream) {
-  if (prepare_kernel(kernel, smem, C) != cudaSuccess) return SV_ERR_CUDA;
+int launch_cluster(K kernel, const Params& P, int nclusters, int C, int threads, int smem,
+                   int max_smem, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  int status = find_prepared(dev, fn, smem, C);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(nclusters) * C, 1, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.gridDim = dim3(C, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -124,9 +165,18 @@ int launch_cluster(K kernel, const Params& P, int nclusters, int C, int smem, cu
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  int active = 0;
-  if (cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) != cudaSuccess) return SV_ERR_CUDA;
-  if (active <= 0) return SV_ERR_UNSUPPORTED;
+  if (status == -1000) {
+    int active = 0;
+    if (prepare_kernel(kernel, max_smem, C) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) != cudaSuccess)
+      status = SV_ERR_CUDA;
+    else
+      status = active > 0 ? active : SV_ERR_UNSUPPORTED;
+    remember_prepared(dev, fn, smem, C, status);
+  }
+  if (status <= 0) return status == 0 ? SV_ERR_UNSUPPORTED : status;
+  const int n = nclusters > 0 ? nclusters : std::min(-nclusters, status);  // status = resident
+  cfg.gridDim = dim3(static_cast<unsigned>(n) * C, 1, 1);
   if (cudaLaunchKernelEx(&cfg, kernel, P) != cudaSuccess) return SV_ERR_CUDA;
   return SV_OK;
 }
@@ -185,6 +235,17 @@ int check_args(const Args& a) {
   return SV_OK;
 }
 
+// Workspace layout: RowRec[N_t] | label partials float[N_t][32] | published
+// pass-1 partials uint64[N_t][32][16] (tag in the upper half of every word).
+size_t ws_cpart_offset(int32_t n_target_rows) {
+  return (static_cast<size_t>(n_target_rows) * sizeof(RowRec) + 255) / 256 * 256;
+}
+
+size_t ws_parts_offset(int32_t n_target_rows) {
+  return ws_cpart_offset(n_target_rows) +
+         (static_cast<size_t>(n_target_rows) * kMaxSlices * sizeof(float) + 255) / 256 * 256;
+}
+
 Params make_params(const Args& a) {
   Params P = {};
   P.tgt = static_cast<const unsigned char*>(a.target_logits);
@@ -210,7 +271,66 @@ Params make_params(const Args& a) {
   P.out_row_stats = a.out_row_stats;
   P.dev_error = a.dev_error;
   P.rec = static_cast<RowRec*>(a.workspace);
+  P.cpart = reinterpret_cast<float*>(static_cast<unsigned char*>(a.workspace) +
+                                     ws_cpart_offset(a.n_target_rows));
+  P.parts = static_cast<unsigned char*>(a.workspace) + ws_parts_offset(a.n_target_rows);
   return P;
+}
+
+// Per-call tag of the published partials: unique within the process, never 0.
+std::atomic<uint32_t> g_tag{0};
+
+uint32_t next_tag() {
+  uint32_t t;
+  do {
+    t = g_tag.fetch_add(1, std::memory_order_relaxed) + 1;
+  } while (t == 0);
+  return t;
+}
+
+// Cooperative launch of one persistent wave: min(units, resident CTAs).
+template <typename K>
+int launch_coop(K kernel, const Params& P, int threads, int smem, const DeviceCache& dc,
+                cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  const void* fn = reinterpret_cast<const void*>(kernel);
+  int per_sm = find_prepared(dev, fn, smem, 0);
+  if (per_sm == -1000) {
+    int n = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             dc.max_smem_optin) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess)
+      per_sm = SV_ERR_CUDA;
+    else
+      per_sm = n > 0 ? n : SV_ERR_UNSUPPORTED;
+    remember_prepared(dev, fn, smem, 0, per_sm);
+  }
+  if (per_sm <= 0) return per_sm == 0 ? SV_ERR_UNSUPPORTED : per_sm;
+  const int grid = std::min(P.nunits, per_sm * dc.sms);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, P) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+template <int ES, int NCW>
+int launch_rows(const Params& P, int smem, const DeviceCache& dc, bool need_z, bool need_conf,
+                bool track, cudaStream_t st) {
+#define SV_ROWS(Z, CF, TR) \
+  launch_coop(rows_kernel<ES, NCW, Z, CF, TR>, P, rows_threads(NCW), smem, dc, st)
+  if (need_conf) return track ? SV_ROWS(true, true, true) : SV_ROWS(true, true, false);
+  if (need_z) return track ? SV_ROWS(true, false, true) : SV_ROWS(true, false, false);
+  return SV_ROWS(false, false, true);
+#undef SV_ROWS
 }
 
 int run_rows(const Args& a) {
@@ -219,26 +339,30 @@ int run_rows(const Args& a) {
   if (rc != SV_OK) return rc;
   Params P = make_params(a);
   const int es = a.dtype == SV_BF16 ? 2 : 4;
-  int smem = 0;
-  const int C = rows_cluster(a.V, es, dc, &smem);
-  if (C < 0) return C;
-  P.S = slice_len(a.V, C, es);
-  P.rowbuf = rowbuf_bytes(P.S, es);
+  RowsGeom geo;
+  rc = rows_geometry(a.V, es, dc, &geo);
+  if (rc != SV_OK) return rc;
+  P.S = geo.L;
+  P.nslices = geo.S;
+  P.nunits = a.n_target_rows * geo.S;
+  P.rowbuf = rowbuf_bytes(geo.L, es);
+  P.nstages = geo.stages;
+  P.tag = next_tag();
+  P.offs_smem = a.B + 1 <= kMaxSmemOffsets;
+  const int smem = geo.smem + (P.offs_smem ? round_up((a.B + 1) * 4, 128) : 0);
+  if (smem > dc.max_smem_optin) return SV_ERR_UNSUPPORTED;
+  // z is needed for sampling, labels and statistics; the exact max / argmax
+  // only for greedy decisions and statistics
   const bool need_z = a.mode == SV_SAMPLE || a.out_conf != nullptr || a.out_row_stats != nullptr;
   const bool need_conf = a.out_conf != nullptr;
+  const bool track = a.mode == SV_GREEDY || a.out_row_stats != nullptr;
+  const int ncw = env_int("SPEC_VERIFY_WARPS", 16) <= 8 ? 8 : 16;
   cudaStream_t st = static_cast<cudaStream_t>(a.stream);
-#define SV_ROWS(ES, Z, CF) launch_cluster(rows_kernel<ES, Z, CF>, P, a.n_target_rows, C, smem, st)
-  if (es == 2) {
-    if (need_conf) rc = SV_ROWS(2, true, true);
-    else if (need_z) rc = SV_ROWS(2, true, false);
-    else rc = SV_ROWS(2, false, false);
-  } else {
-    if (need_conf) rc = SV_ROWS(4, true, true);
-    else if (need_z) rc = SV_ROWS(4, true, false);
-    else rc = SV_ROWS(4, false, false);
-  }
-#undef SV_ROWS
-  return rc;
+  if (es == 2)
+    return ncw == 8 ? launch_rows<2, 8>(P, smem, dc, need_z, need_conf, track, st)
+                    : launch_rows<2, 16>(P, smem, dc, need_z, need_conf, track, st);
+  return ncw == 8 ? launch_rows<4, 8>(P, smem, dc, need_z, need_conf, track, st)
+                  : launch_rows<4, 16>(P, smem, dc, need_z, need_conf, track, st);
 }
 
 int run_finalize(const Args& a) {
@@ -247,10 +371,14 @@ int run_finalize(const Args& a) {
   if (rc != SV_OK) return rc;
   Params P = make_params(a);
   const int es = a.dtype == SV_BF16 ? 2 : 4;
+  RowsGeom geo;
+  rc = rows_geometry(a.V, es, dc, &geo);
+  if (rc != SV_OK) return rc;
+  P.nslices = geo.S;
   cudaStream_t st = static_cast<cudaStream_t>(a.stream);
   const bool filtered = P.top_k > 0 || P.top_p < 1.f;
   if (a.mode == SV_GREEDY || filtered) {
-    finalize_select_kernel<<<(a.B + kThreads - 1) / kThreads, kThreads, 0, st>>>(P);
+    finalize_select_kernel<<<(a.B + kWarps - 1) / kWarps, kThreads, 0, st>>>(P);
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
   }
   int smem = 0;
@@ -258,8 +386,11 @@ int run_finalize(const Args& a) {
   if (C4 < 0) return C4;
   P.S4 = slice_len(a.V, C4, es);
   P.rowbuf4 = rowbuf_bytes(P.S4, es);
-  if (es == 2) return launch_cluster(finalize_draw_kernel<2>, P, a.B, C4, smem, st);
-  return launch_cluster(finalize_draw_kernel<4>, P, a.B, C4, smem, st);
+  if (es == 2)
+    return launch_cluster(finalize_draw_kernel<2>, P, a.B, C4, kThreads, smem, dc.max_smem_optin,
+                          st);
+  return launch_cluster(finalize_draw_kernel<4>, P, a.B, C4, kThreads, smem, dc.max_smem_optin,
+                        st);
 }
 
 }  // namespace
@@ -282,8 +413,9 @@ extern "C" {
 
 size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows) {
   (void)B;
-  const size_t rows = n_target_rows > 0 ? static_cast<size_t>(n_target_rows) : 0;
-  const size_t bytes = rows * sizeof(sv::RowRec);
+  const int32_t rows = n_target_rows > 0 ? n_target_rows : 0;
+  const size_t bytes = sv::ws_parts_offset(rows) +
+                       static_cast<size_t>(rows) * sv::kMaxSlices * sv::kPartWords * 8;
   return (bytes + 255) / 256 * 256 + 256;
 }
 
@@ -319,7 +451,7 @@ const char* spec_verify_status_string(int status) {
   }
 }
 
-int spec_verify_cluster_size(int32_t V, int32_t dtype, int32_t top_k, float top_p) {
+int spec_verify_slices_per_row(int32_t V, int32_t dtype, int32_t top_k, float top_p) {
   (void)top_k;
   (void)top_p;
   if (V <= 0) return SV_ERR_ARG;
@@ -327,8 +459,9 @@ int spec_verify_cluster_size(int32_t V, int32_t dtype, int32_t top_k, float top_
   sv::DeviceCache dc;
   const int rc = sv::device_info(&dc);
   if (rc != SV_OK) return rc;
-  int smem = 0;
-  return sv::rows_cluster(V, dtype == SV_BF16 ? 2 : 4, dc, &smem);
+  sv::RowsGeom geo;
+  const int g = sv::rows_geometry(V, dtype == SV_BF16 ? 2 : 4, dc, &geo);
+  return g != SV_OK ? g : geo.S;
 }
 
 }  // extern "C"

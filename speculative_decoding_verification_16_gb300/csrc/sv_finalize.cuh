@@ -52,16 +52,31 @@ __device__ __forceinline__ ReqInfo scan_request(const Params& P, int32_t r) {
   return q;
 }
 
-// Weight of token v for the final draw: residual max(0, p_t - p_d), or p_t.
+// Weight of token v for the final draw, in units of 1 / z_t: the residual
+// max(0, p_t - p_d) * z_t = max(0, 2^a - (z_t / z_d) 2^b), or p_t * z_t = 2^a,
+// with a = t sc - h_t and b = d sc - h_d.
 struct DrawRow {
-  float lt, ld, sc;  // log2 normalisers: lt = mt * sc + log2(zt)
+  float ht, hd, ratio, sc;  // references and z_t / z_d
   bool residual;
   __device__ __forceinline__ float w(float t, float d) const {
-    const float pt = ex2(fmaf(t, sc, -lt));
+    const float pt = ex2(fmaf(t, sc, -ht));
     if (!residual) return pt;
-    return fmaxf(0.f, pt - ex2(fmaf(d, sc, -ld)));
+    return fmaxf(0.f, pt - ratio * ex2(fmaf(d, sc, -hd)));
   }
 };
+
+// c* of every drafted row of request r: the rows kernel's per-slice partials
+// summed in slice order.  Lanes of one warp take one row each.
+__device__ __forceinline__ void sum_labels(const Params& P, int32_t r, int32_t off, int32_t ell,
+                                           int lane) {
+  if (P.out_conf == nullptr) return;
+  for (int32_t j = lane; j < ell - 1; j += 32) {
+    const float* cp = P.cpart + static_cast<size_t>(off + j) * 32;
+    float c = 0.f;
+    for (int q = 0; q < P.nslices; ++q) c += cp[q];
+    P.out_conf[off - r + j] = c;
+  }
+}
 
 // Inclusive warp scan of v over lanes.
 __device__ __forceinline__ float warp_incl_scan(float v) {
@@ -135,15 +150,18 @@ __global__ void __launch_bounds__(kThreads) finalize_draw_kernel(const Params P)
     if (s_t.nbytes) bulk_g2s(smem_addr(buf_t), s_t.gsrc, s_t.nbytes, bar);
     if (s_d.nbytes) bulk_g2s(smem_addr(buf_d), s_d.gsrc, s_d.nbytes, bar);
   }
-  const bool timeout = !mbar_wait_bounded(bar, 0, kSpinLimit);
+  bool timeout = false;
+  mbar_wait(bar, 0, timeout);
   const bool any_timeout = __syncthreads_or(timeout ? 1 : 0) != 0;
 
   const float sc = P.sc;
   DrawRow dr;
   dr.sc = sc;
-  dr.lt = fmaf(rr.mt, sc, __log2f(rr.zt));
-  dr.ld = fmaf(rr.md, sc, __log2f(rr.zd));
+  dr.ht = rr.mt;
+  dr.hd = rr.md;
+  dr.ratio = rr.zt / rr.zd;
   dr.residual = q.residual;
+  if (rank == 0 && (tid >> 5) == 1) sum_labels(P, r, q.off, q.ell, tid & 31);
   const int32_t E = (s_t.len + kThreads - 1) / kThreads;  // elements per thread
   const int32_t i0 = min(s_t.len, tid * E), i1 = min(s_t.len, i0 + E);
   const float u = __ldg(P.uniforms + q.off + q.ell - 1);
@@ -245,18 +263,25 @@ __global__ void __launch_bounds__(kThreads) finalize_draw_kernel(const Params P)
     for (int32_t j = 0; j <= q.a && j < q.ell; ++j) flags |= P.rec[q.off + j].flags;
     if (flags) raise_error(P, flags);
   }
-  if (any_timeout) mbar_wait_bounded(bar, 0, kSpinLimit);
+  if (any_timeout) {  // one more bounded wait for a copy still in flight
+    bool again = false;
+    mbar_wait(bar, 0, again);
+  }
 }
 
 // Greedy and filtered sampling: the final token is already known per row.
+// One warp per request: lane 0 scans and writes, all lanes sum labels.
 __global__ void __launch_bounds__(kThreads) finalize_select_kernel(const Params P) {
-  const int32_t r = blockIdx.x * kThreads + threadIdx.x;
+  const int32_t r = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (r >= P.B) return;
   const ReqInfo q = scan_request(P, r);
   if (!q.ok) {
-    raise_error(P, SV_DEVERR_LEN);
+    if (lane == 0) raise_error(P, SV_DEVERR_LEN);
     return;
   }
+  sum_labels(P, r, q.off, q.ell, lane);
+  if (lane != 0) return;
   const RowRec& fr = P.rec[q.off + q.a];
   const int32_t final_tok = P.mode == SV_GREEDY ? fr.argt : fr.pick;
   P.out_accept_len[r] = q.a;

@@ -29,24 +29,50 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// Plain arrival (release at CTA scope: prior shared-memory writes of this
+// thread are visible to a thread that then observes the phase completion).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// One wait attempt.  The hint lets the hardware suspend the thread (instead
+// of spinning on the issue slot) until the phase completes or ~0.5 ms pass.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(500000u)
       : "memory");
   return ok != 0;
 }
 
-// Wait for phase `parity` of the barrier; gives up after `limit` polls and
-// returns false (the caller records a timeout instead of hanging).
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Time limit of one bounded wait.  A kernel that has already timed out once
+// polls each later barrier only once, so that it drains quickly.
+constexpr uint64_t kWaitLimitNs = 200ull * 1000 * 1000;
+
+// Wait for the completion of phase `parity` of the barrier.  Gives up after
+// kWaitLimitNs and sets `timed_out` (the caller reports a timeout instead of
+// hanging).
+__device__ __forceinline__ void mbar_wait(uint32_t bar, uint32_t parity, bool& timed_out) {
+  if (mbar_try_wait(bar, parity)) return;
+  if (timed_out) return;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 3) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) {
+      timed_out = true;
+      return;
+    }
+  }
 }
 
 // Non-tensor bulk copy global -> this CTA's shared memory.  dst, src and
@@ -58,6 +84,21 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
           dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
+}
+
+// 4-byte asynchronous global -> shared copy (cp.async, L1-allocating), and
+// its commit / wait groups (hardware waits: they always complete).
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---------------------------------------------------------------- clusters
@@ -96,6 +137,17 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+
+// 16-byte store into a cluster peer's shared memory that completes 16
+// transaction bytes on the peer's mbarrier `rbar` (both addresses from mapa).
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t rbar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+          raddr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
+      : "memory");
 }
 
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {

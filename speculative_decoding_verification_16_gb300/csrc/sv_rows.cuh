@@ -1,23 +1,48 @@
 // sv_rows.cuh -- the bandwidth-bound rows kernel (no top-k / top-p filter).
 //
-// One thread-block cluster of C CTAs per target row g.  CTA `rank` owns the
-// vocabulary slice [rank * S, rank * S + S) of target row g and, when row g
-// scores a drafted token, of its draft partner row.  The slice pair is
-// brought from HBM into the CTA's shared memory once, with bulk copies in
-// kChunks pieces so that the statistics pass starts on the first piece
-// while the rest is still in flight.
+// One persistent cooperative grid, one CTA per SM, every SM busy.  Each
+// logits row is cut into S slices of at most L elements; work unit
+// u = (target row g, slice k), u = g * S + k, and CTA c handles units
+// u = c, c + N, c + 2N, ... (N CTAs), so the S slices of a row are handled in
+// the same round by S different CTAs.  A unit's slice pair (target slice and,
+// when row g scores a drafted token, the draft partner's slice) is brought
+// into one of NS shared-memory stages by bulk copies (cp.async.bulk) and
+// stays there for both passes: each logit crosses HBM once.  The CTAs holding
+// the slices of one row exchange their partial statistics through an
+// L2-resident workspace slot per (row, slice) (all CTAs of a cooperative
+// launch are co-resident; every wait is time-bounded).  Every published
+// 32-bit word travels in a 64-bit word together with a per-call tag (relaxed
+// 64-bit accesses are single-copy atomic), so a reader checks each word
+// itself: no release/acquire pair, one L2 round trip per poll.
 //
-//  pass 1 (as pieces land): per-thread online max / sum exp / argmax of both
-//         rows (log-sum-exp merge algebra), then a CTA merge;
-//  exchange: every CTA stores its partial record into every other CTA's
-//         shared memory (distributed shared memory), one cluster barrier,
-//         then every CTA merges the C records in rank order;
-//  pass 2 (only when labels are requested): c* = sum_v min(p_t(v), p_d(v))
-//         = 1 - 1/2 ||p_t - p_d||_1 over the resident slice, one exp2 per
-//         element pair: min(p_t, p_d) = exp2(min(log2 p_t, log2 p_d));
-//         partial sums go to CTA 0 through distributed shared memory;
-//  epilogue (CTA 0): row statistics, label, accept decision of the drafted
-//         token -- sampling: u * p_d(x) < p_t(x), greedy: x == argmax_t.
+// Warp roles (mbarriers between them; no CTA-wide barrier in the loop):
+//  * NCW consumer warps: pass 1 of unit i, then pass 2 of unit i - kDelay;
+//  * producer warp: refills a stage once every role has released it (row
+//    metadata arrives by cp.async on the stage's `full` mbarrier) and writes
+//    the unit's label partial;
+//  * kPublishers publisher warps (unit i by warp i % kPublishers): merge the
+//    consumer warps' pass-1 partials of a unit into the CTA partial and
+//    publish it;
+//  * kGatherers gatherer warps (unit j by warp j % kGatherers): wait for the
+//    S partials of the unit's row, merge them into the row statistics for
+//    pass 2, and for the row's first slice run the row epilogue (accept
+//    decision, statistics).
+//
+// Per unit:
+//  pass 1   sums kept as sum_v 2^(x_v * sc) = s * 2^h, sc = log2(e) / T: each
+//           term is exp2(fma(x, sc, -h)) for a fixed reference h, so rounding
+//           is relative to the (small) exponent itself, whatever T is.  The
+//           running max / argmax is tracked only when needed (greedy
+//           decisions, row statistics).  Partials merge as max h, one rescale
+//           by exp2(h - H) per partial, then a plain sum.
+//  pass 2   (labels only) c* = sum_v min(p_t(v), p_d(v)) = 1 - 1/2 ||p_t - p_d||_1
+//           over the resident slice pair, one exp2 per element pair:
+//           min(p_t, p_d) * s_t = exp2(min(a, b - delta)), a = fma(t, sc, -h_t),
+//           b = fma(d, sc, -h_d), delta = log2(s_d / s_t).  One partial per
+//           unit goes to the workspace; the finalize kernel sums a row's S
+//           partials in slice order.
+//  epilogue accept decision of the drafted token -- sampling:
+//           u * p_d(x) < p_t(x), greedy: x == argmax_t -- and row statistics.
 //
 // Confidence label: DSpark tutorial, "置信度预测头".  Accept rule and the
 // first-rejection structure: DSpark tutorial, "推测解码的两步流程"; DFlash /
@@ -28,101 +53,226 @@
 
 namespace sv {
 
-// Shared-memory header layout of the rows kernel (bytes from the base).
-constexpr int kOffBars = 0;                                   // kChunks mbarriers
-constexpr int kOffRecs = 64;                                  // kMaxCluster records
-constexpr int kOffCpart = kOffRecs + kMaxCluster * kRecWords * 4;  // kMaxCluster floats
-constexpr int kOffScratch = kOffCpart + kMaxCluster * 4;      // reduction scratch
-constexpr int kOffInfo = kOffScratch + 64 * 4;                // per-CTA row info
-static_assert(kOffInfo + 64 <= kHdrBytes, "rows kernel header");
+constexpr int kMaxStages = 6;
+constexpr int kDelay = 3;             // pass 2 of unit i - kDelay follows pass 1 of unit i
+constexpr int kMaxConsumerWarps = 16;
+constexpr int kPublishers = 2;
+constexpr int kGatherers = 4;
+constexpr int kMaxSlices = 32;        // slices per row (gatherer lanes)
+constexpr int kPartWords = 16;        // 64-bit words per published partial (12 used)
+constexpr int kMaxSmemOffsets = 4096; // row_offsets entries kept in shared memory
 
-// Record word layout.
-enum { R_MT = 0, R_ST, R_IT, R_MD, R_SD, R_ID, R_XT, R_XD, R_HASX, R_BAD };
+// Shared-memory header layout of the rows kernel (bytes from the base).
+constexpr int kOffFull = 0;                                   // kMaxStages mbarriers each
+constexpr int kOffEmpty = kOffFull + 8 * kMaxStages;
+constexpr int kOffPartBar = kOffEmpty + 8 * kMaxStages;
+constexpr int kOffStatsBar = kOffPartBar + 8 * kMaxStages;
+constexpr int kOffPart = 256;                                 // [stage][warp][16] words
+constexpr int kOffCp = kOffPart + kMaxStages * kMaxConsumerWarps * 64;  // [stage][warp] floats
+constexpr int kOffStats = kOffCp + kMaxStages * kMaxConsumerWarps * 4;  // [stage][8] words
+constexpr int kOffInfo = kOffStats + kMaxStages * 32;                   // [stage] RowInfo
+constexpr int kRowsHdrBytes = 8192;
+static_assert(kOffStatsBar + 8 * kMaxStages <= kOffPart, "rows kernel barriers");
+static_assert(kOffInfo + kMaxStages * 64 <= kRowsHdrBytes, "rows kernel header");
+
+// Partial / record word layout.
+enum { R_HT = 0, R_ST, R_MT, R_IT, R_HD, R_SD, R_MD, R_ID, R_BAD, R_XT, R_XD, R_HASX, R_NWORDS };
 
 struct RowInfo {
-  int32_t r, j, pair, gd, x, ok, tokok, pad;
+  int32_t g, k, r, off, off1, pair, gd;
+  int32_t x;    // drafted token (cp.async)
+  int32_t ell;  // l_r (cp.async)
+  float u;      // uniform of the row (cp.async)
+  int32_t pad[6];
+};
+static_assert(sizeof(RowInfo) == 64, "RowInfo layout");
+
+// Partial statistics of a row: sum_v 2^(x_v * sc) = s * 2^h; m = max raw
+// logit and i = lowest id holding it (tracked variant only; m = -inf, i =
+// INT_MAX otherwise).
+struct RStat {
+  float h, s, m;
+  int32_t i;
 };
 
-// Locate request r of target row g (largest r with offs[r] <= g) and check
-// the request's layout.
-__device__ __forceinline__ RowInfo locate_row(const Params& P, int32_t g) {
-  RowInfo info{};
-  int32_t lo = 0, hi = P.B - 1;
-  while (lo < hi) {
-    const int32_t mid = (lo + hi + 1) >> 1;
-    if (__ldg(P.offs + mid) <= g) lo = mid; else hi = mid - 1;
-  }
-  const int32_t r = lo;
-  const int32_t off = __ldg(P.offs + r), off1 = __ldg(P.offs + r + 1);
-  const int32_t ell = __ldg(P.lens + r);
-  info.r = r;
-  info.j = g - off;
-  info.ok = off <= g && g < off1 && off1 - off == ell && ell >= 1 && ell <= P.max_len && off >= r;
-  info.gd = g - r;
-  info.pair = info.ok && info.j < ell - 1 && info.gd >= 0 && info.gd < P.Nd;
-  info.x = info.pair ? __ldg(P.draft_tokens + info.gd) : -1;
-  info.tokok = info.x >= 0 && info.x < P.V;
-  return info;
+__device__ __forceinline__ RStat rstat_empty() {
+  return RStat{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
 }
 
-// Pass-1 update of one thread's statistics with VEC elements of one vector.
-template <int VEC, bool NEED_Z>
-__device__ __forceinline__ void stat_update(Stat& st, float& nm, const float* x, int32_t id0,
-                                            float sc, bool& bad) {
-  float vmax = x[0];
-#pragma unroll
-  for (int l = 1; l < VEC; ++l) vmax = fmax_nan(vmax, x[l]);
-  bad |= (vmax != vmax);
-  if (vmax > st.m) {
-    if (NEED_Z) st.s *= ex2((st.m - vmax) * sc);
-    st.m = vmax;
-    nm = vmax * sc;
-    int l0 = VEC - 1;
-#pragma unroll
-    for (int l = VEC - 2; l >= 0; --l)
-      if (x[l] == vmax) l0 = l;
-    st.i = id0 + l0;
-  }
-  if (NEED_Z && st.m > -INFINITY) {
-    float e[VEC];
-#pragma unroll
-    for (int l = 0; l < VEC; ++l) e[l] = ex2(fmaf(x[l], sc, -nm));
-#pragma unroll
-    for (int w = VEC / 2; w > 0; w >>= 1)
-#pragma unroll
-      for (int l = 0; l < w; ++l) e[l] += e[l + w];
-    st.s += e[0];
-  }
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
-// Pass 1 over the vectors [k0, k1) of a slice buffer, strided by the block.
-template <int ES, bool NEED_Z>
-__device__ __forceinline__ void stats_range(const unsigned char* buf, const Slice& s, int32_t k0,
-                                            int32_t k1, float sc, Stat& st, float& nm, bool& bad) {
+__device__ __forceinline__ float warp_sum_f32(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Merge the 32 lanes' partials: max reference, one rescale each, plain sum;
+// argmax = lowest id among lanes holding the largest maximum.  Every lane
+// gets the same bits.
+__device__ __forceinline__ RStat rstat_warp_reduce(const RStat& a) {
+  RStat r;
+  r.h = warp_max_f32(a.h);
+  const float part = (a.h == -INFINITY) ? 0.f : a.s * ex2(a.h - r.h);
+  r.s = r.h == -INFINITY ? 0.f : warp_sum_f32(part);
+  r.m = warp_max_f32(a.m);
+  r.i = __reduce_min_sync(0xffffffffu, a.m == r.m ? a.i : 0x7fffffff);
+  return r;
+}
+
+template <int VEC>
+__device__ __forceinline__ float vmax_nan(const float* x) {
+  float v = x[0];
+#pragma unroll
+  for (int l = 1; l < VEC; ++l) v = fmax_nan(v, x[l]);
+  return v;
+}
+
+template <int VEC>
+__device__ __forceinline__ float sum_exp2(const float* x, float sc, float h) {
+  float e[VEC];
+#pragma unroll
+  for (int l = 0; l < VEC; ++l) e[l] = ex2(fmaf(x[l], sc, -h));
+#pragma unroll
+  for (int w = VEC / 2; w > 0; w >>= 1)
+#pragma unroll
+    for (int l = 0; l < w; ++l) e[l] += e[l + w];
+  return e[0];
+}
+
+// Pass 1 of one consumer thread over its vectors k = ct, ct + NCT, ... of a
+// slice.  TRACK: exact running max / argmax.  Otherwise the reference h is
+// taken from the thread's first vector holding a finite value; an overflow or
+// a non-finite input sends the thread to the tracked variant (rare).
+template <int ES, int NCT, bool NEED_Z, bool TRACK>
+__device__ __forceinline__ RStat pass1_thread(const unsigned char* buf, const Slice& s, float sc,
+                                              int ct, bool& bad) {
   constexpr int VEC = 16 / ES;
-  for (int32_t k = k0 + threadIdx.x; k < k1; k += kThreads) {
+  const int32_t nv = s.nbytes >> 4;
+  const int32_t idbase = s.v0 - s.hoff;
+  RStat st = rstat_empty();
+  int32_t k = ct;
+  if (!TRACK) {
+    for (; k < nv; k += NCT) {  // first vector with a finite maximum
+      float x[VEC];
+      load_vec<ES>(buf, s, k, x);
+      const float vm = vmax_nan<VEC>(x);
+      if (vm != vm || vm == INFINITY) break;  // non-finite: tracked variant below
+      if (vm > -INFINITY) {
+        st.h = vm * sc;
+        break;
+      }
+    }
+    if (st.h > -INFINITY) {
+#pragma unroll 2
+      for (; k < nv; k += NCT) {
+        float x[VEC];
+        load_vec<ES>(buf, s, k, x);
+        st.s += sum_exp2<VEC>(x, sc, st.h);
+      }
+      if (st.s < INFINITY) return st;  // finite: done
+    } else if (k >= nv) {
+      return st;  // nothing but -inf in this thread's vectors
+    }
+    st = rstat_empty();  // overflow or non-finite input
+  }
+  for (k = ct; k < nv; k += NCT) {
     float x[VEC];
     load_vec<ES>(buf, s, k, x);
-    stat_update<VEC, NEED_Z>(st, nm, x, s.v0 + k * VEC - s.hoff, sc, bad);
+    const float vm = vmax_nan<VEC>(x);
+    if (!(vm <= st.m)) {  // new maximum, or NaN
+      if (vm != vm) {
+        bad = true;
+      } else {
+        const float nh = vm * sc;
+        if (NEED_Z && st.h > -INFINITY) st.s *= ex2(st.h - nh);
+        st.h = nh;
+        st.m = vm;
+        int l0 = VEC - 1;
+#pragma unroll
+        for (int l = VEC - 2; l >= 0; --l)
+          if (x[l] == vm) l0 = l;
+        st.i = idbase + k * VEC + l0;
+      }
+    }
+    if (NEED_Z && st.h > -INFINITY) st.s += sum_exp2<VEC>(x, sc, st.h);
   }
+  if (st.m == INFINITY) bad = true;
+  return st;
 }
 
-// Pass 2: partial sum of exp2(min(t * sc - lt, d * sc - ld)) over the slice.
-template <int ES>
-__device__ __forceinline__ float overlap_range(const unsigned char* bt, const Slice& st_,
-                                               const unsigned char* bd, const Slice& sd_,
-                                               float sc, float lt, float ld) {
+// Pass 1 fast path for a slice pair on one vector grid with no masked lanes
+// and no need for the exact max: both rows in one loop, the references taken
+// from the thread's first vector of each row.  Returns false (the caller then
+// runs the general path) on a non-finite input or an overflow.
+template <int ES, int NCT>
+__device__ __forceinline__ bool pass1_pair_fast(const unsigned char* bt, const unsigned char* bd,
+                                                int32_t nv, float sc, int ct, RStat& at,
+                                                RStat& ad) {
+  constexpr int VEC = 16 / ES;
+  at = rstat_empty();
+  ad = rstat_empty();
+  int32_t k = ct;
+  if (k >= nv) return true;
+  float t[VEC], d[VEC];
+  load_vec_raw<ES>(bt, k, t);
+  load_vec_raw<ES>(bd, k, d);
+  const float mt = vmax_nan<VEC>(t), md = vmax_nan<VEC>(d);
+  if (!(mt > -INFINITY && mt < INFINITY && md > -INFINITY && md < INFINITY)) return false;
+  const float ht = mt * sc, hd = md * sc;
+  float st = sum_exp2<VEC>(t, sc, ht), sd = sum_exp2<VEC>(d, sc, hd);
+#pragma unroll 2
+  for (k += NCT; k < nv; k += NCT) {
+    load_vec_raw<ES>(bt, k, t);
+    load_vec_raw<ES>(bd, k, d);
+    st += sum_exp2<VEC>(t, sc, ht);
+    sd += sum_exp2<VEC>(d, sc, hd);
+  }
+  if (!(st < INFINITY && sd < INFINITY)) return false;
+  at = RStat{ht, st, -INFINITY, 0x7fffffff};
+  ad = RStat{hd, sd, -INFINITY, 0x7fffffff};
+  return true;
+}
+
+// Pass 2 of one consumer thread: sum of exp2(min(a, b - delta)) over its vectors.
+template <int ES, int NCT>
+__device__ __forceinline__ float pass2_thread(const unsigned char* bt, const Slice& st_,
+                                              const unsigned char* bd, const Slice& sd_, float sc,
+                                              float ht, float hd, float delta, int ct) {
   constexpr int VEC = 16 / ES;
   float acc = 0.f;
-  if (st_.hoff == sd_.hoff) {  // same vector grid: vectorised
+  if (slice_aligned<ES>(st_) && slice_aligned<ES>(sd_)) {  // no masked lanes
     const int32_t nv = st_.nbytes >> 4;
-    for (int32_t k = threadIdx.x; k < nv; k += kThreads) {
+#pragma unroll 2
+    for (int32_t k = ct; k < nv; k += NCT) {
+      float t[VEC], d[VEC];
+      load_vec_raw<ES>(bt, k, t);
+      load_vec_raw<ES>(bd, k, d);
+      float e[VEC];
+#pragma unroll
+      for (int l = 0; l < VEC; ++l)
+        e[l] = ex2(fminf(fmaf(t[l], sc, -ht), fmaf(d[l], sc, -hd) - delta));
+#pragma unroll
+      for (int w = VEC / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int l = 0; l < w; ++l) e[l] += e[l + w];
+      acc += e[0];
+    }
+  } else if (st_.hoff == sd_.hoff) {  // same vector grid: vectorised, masked ends
+    const int32_t nv = st_.nbytes >> 4;
+#pragma unroll 2
+    for (int32_t k = ct; k < nv; k += NCT) {
       float t[VEC], d[VEC];
       load_vec<ES>(bt, st_, k, t);
       load_vec<ES>(bd, sd_, k, d);
       float e[VEC];
 #pragma unroll
-      for (int l = 0; l < VEC; ++l) e[l] = ex2(fminf(fmaf(t[l], sc, -lt), fmaf(d[l], sc, -ld)));
+      for (int l = 0; l < VEC; ++l)
+        e[l] = ex2(fminf(fmaf(t[l], sc, -ht), fmaf(d[l], sc, -hd) - delta));
 #pragma unroll
       for (int w = VEC / 2; w > 0; w >>= 1)
 #pragma unroll
@@ -130,165 +280,379 @@ __device__ __forceinline__ float overlap_range(const unsigned char* bt, const Sl
       acc += e[0];
     }
   } else {  // rows with different 16-byte phase (V * esize not a multiple of 16)
-    for (int32_t i = threadIdx.x; i < st_.len; i += kThreads) {
+    for (int32_t i = ct; i < st_.len; i += NCT) {
       const float t = slice_elem<ES>(bt, st_, i), d = slice_elem<ES>(bd, sd_, i);
-      acc += ex2(fminf(fmaf(t, sc, -lt), fmaf(d, sc, -ld)));
+      acc += ex2(fminf(fmaf(t, sc, -ht), fmaf(d, sc, -hd) - delta));
     }
   }
   return acc;
 }
 
-template <int ES, bool NEED_Z, bool NEED_CONF>
-__global__ void __launch_bounds__(kThreads) rows_kernel(const Params P) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t csize = cluster_nctarank();
-  const int32_t g = static_cast<int32_t>(cluster_id_x());
-  const int tid = threadIdx.x;
-  float* recs = reinterpret_cast<float*>(smem + kOffRecs);
-  float* cpart = reinterpret_cast<float*>(smem + kOffCpart);
-  float* scratch = reinterpret_cast<float*>(smem + kOffScratch);
-  RowInfo* sinfo = reinterpret_cast<RowInfo*>(smem + kOffInfo);
-  unsigned char* buf_t = smem + kHdrBytes;
-  unsigned char* buf_d = buf_t + P.rowbuf;
-  const uint32_t bar0 = smem_addr(smem + kOffBars);
-
-  cluster_arrive_relaxed();  // this CTA has started (completed before the first DSMEM store)
-
-  if (tid == 0) {
-    *sinfo = locate_row(P, g);
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) mbar_init(bar0 + 8 * c, 1);
-    fence_mbar_init();
+// Locate request r of target row g (largest r with offs[r] <= g) in the
+// row_offsets array (a shared-memory copy when it fits).
+__device__ __forceinline__ void locate_row(const Params& P, const int32_t* offs, int32_t g,
+                                           RowInfo* info) {
+  int32_t lo = 0, hi = P.B - 1;
+  while (lo < hi) {
+    const int32_t mid = (lo + hi + 1) >> 1;
+    if (offs[mid] <= g) lo = mid; else hi = mid - 1;
   }
-  __syncthreads();
-  const RowInfo info = *sinfo;
+  info->g = g;
+  info->r = lo;
+  info->off = offs[lo];
+  info->off1 = offs[lo + 1];
+  info->gd = g - lo;
+  info->pair = info->off <= g && g < info->off1 - 1 && info->gd >= 0 && info->gd < P.Nd;
+  info->x = -1;
+  info->ell = 0;
+}
 
-  const unsigned char* trow = P.tgt + static_cast<size_t>(g) * P.V * ES;
-  const unsigned char* drow = P.drf + static_cast<size_t>(info.gd) * P.V * ES;
-  const Slice s_t = make_slice<ES>(trow, P.V, rank, P.S);
-  Slice s_d = make_slice<ES>(drow, P.V, rank, P.S);
-  if (!info.pair) s_d.nbytes = 0, s_d.len = 0;
+template <int ES>
+__device__ __forceinline__ Slice target_slice(const Params& P, const RowInfo& info) {
+  return make_slice<ES>(P.tgt + static_cast<size_t>(info.g) * P.V * ES, P.V, info.k, P.S);
+}
 
-  if (tid == 0) {
-    for (int c = 0; c < kChunks; ++c) {
-      int32_t tlo, thi, dlo, dhi;
-      chunk_range(s_t.nbytes, c, &tlo, &thi);
-      chunk_range(s_d.nbytes, c, &dlo, &dhi);
-      const uint32_t bar = bar0 + 8 * c;
-      mbar_arrive_expect_tx(bar, static_cast<uint32_t>((thi - tlo) + (dhi - dlo)));
-      if (thi > tlo) bulk_g2s(smem_addr(buf_t + tlo), s_t.gsrc + tlo, thi - tlo, bar);
-      if (dhi > dlo) bulk_g2s(smem_addr(buf_d + dlo), s_d.gsrc + dlo, dhi - dlo, bar);
-    }
+template <int ES>
+__device__ __forceinline__ Slice draft_slice(const Params& P, const RowInfo& info) {
+  if (!info.pair) return Slice{nullptr, 0, 0, 0, info.k * P.S};
+  return make_slice<ES>(P.drf + static_cast<size_t>(info.gd) * P.V * ES, P.V, info.k, P.S);
+}
+
+struct RowsSmem {
+  unsigned char* base;
+  int32_t rowbuf;
+  __device__ __forceinline__ uint32_t full(int s) const { return smem_addr(base + kOffFull + 8 * s); }
+  __device__ __forceinline__ uint32_t empty(int s) const { return smem_addr(base + kOffEmpty + 8 * s); }
+  __device__ __forceinline__ uint32_t partbar(int s) const {
+    return smem_addr(base + kOffPartBar + 8 * s);
   }
+  __device__ __forceinline__ uint32_t statsbar(int s) const {
+    return smem_addr(base + kOffStatsBar + 8 * s);
+  }
+  __device__ __forceinline__ float* part(int s, int w) const {
+    return reinterpret_cast<float*>(base + kOffPart) + (s * kMaxConsumerWarps + w) * 16;
+  }
+  __device__ __forceinline__ float* cp(int s) const {
+    return reinterpret_cast<float*>(base + kOffCp) + s * kMaxConsumerWarps;
+  }
+  __device__ __forceinline__ float* stats(int s) const {
+    return reinterpret_cast<float*>(base + kOffStats) + s * 8;
+  }
+  __device__ __forceinline__ RowInfo* info(int s) const {
+    return reinterpret_cast<RowInfo*>(base + kOffInfo) + s;
+  }
+  __device__ __forceinline__ unsigned char* tbuf(int s) const {
+    return base + kRowsHdrBytes + s * 2 * rowbuf;
+  }
+  __device__ __forceinline__ unsigned char* dbuf(int s) const { return tbuf(s) + rowbuf; }
+};
 
-  // ---- pass 1: statistics while the pieces land
+// Producer step (one lane): load unit u into stage s.  The stage's `full`
+// barrier completes when the bulk copies' bytes have landed and the row
+// metadata copied by cp.async has arrived.
+template <int ES>
+__device__ __forceinline__ void produce_unit(const Params& P, const RowsSmem& sm,
+                                             const int32_t* offs, int32_t u, int s) {
+  RowInfo* info = sm.info(s);
+  locate_row(P, offs, u / P.nslices, info);
+  info->k = u % P.nslices;
+  const RowInfo cur = *info;
+  const Slice st = target_slice<ES>(P, cur);
+  const Slice sd = draft_slice<ES>(P, cur);
+  const uint32_t bar = sm.full(s);
+  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(st.nbytes + sd.nbytes));
+  if (st.nbytes) bulk_g2s(smem_addr(sm.tbuf(s)), st.gsrc, st.nbytes, bar);
+  if (sd.nbytes) bulk_g2s(smem_addr(sm.dbuf(s)), sd.gsrc, sd.nbytes, bar);
+  cp_async4(smem_addr(&info->u), P.uniforms + cur.g);
+  cp_async4(smem_addr(&info->ell), P.lens + cur.r);
+  if (cur.pair) cp_async4(smem_addr(&info->x), P.draft_tokens + cur.gd);
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Threads of the rows kernel: NCW consumer warps, producer, publishers, gatherers.
+constexpr int rows_threads(int ncw) { return (ncw + 1 + kPublishers + kGatherers) * 32; }
+
+template <int ES, int NCW, bool NEED_Z, bool NEED_CONF, bool TRACK>
+__global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params P) {
+  static_assert(NCW <= kMaxConsumerWarps, "consumer warps");
+  constexpr int NCT = NCW * 32;
+  constexpr int W_PROD = NCW, W_PUB = NCW + 1, W_GATH = NCW + 1 + kPublishers;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  const RowsSmem sm{smem_raw, P.rowbuf};
+  const int32_t N = static_cast<int32_t>(gridDim.x);
+  const int32_t c = static_cast<int32_t>(blockIdx.x);
+  const int32_t n_units = P.nunits > c ? (P.nunits - c + N - 1) / N : 0;
+  const int NS = P.nstages;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float sc = P.sc;
-  Stat st_t = stat_empty(), st_d = stat_empty();
-  float nm_t = 0.f, nm_d = 0.f;
-  bool bad = false, timeout = false;
-  for (int c = 0; c < kChunks; ++c) {
-    if (!mbar_wait_bounded(bar0 + 8 * c, 0, kSpinLimit)) timeout = true;
-    int32_t lo, hi;
-    chunk_range(s_t.nbytes, c, &lo, &hi);
-    stats_range<ES, NEED_Z>(buf_t, s_t, lo >> 4, hi >> 4, sc, st_t, nm_t, bad);
-    if (info.pair) {
-      chunk_range(s_d.nbytes, c, &lo, &hi);
-      stats_range<ES, NEED_Z>(buf_d, s_d, lo >> 4, hi >> 4, sc, st_d, nm_d, bad);
-    }
-  }
-  const bool any_bad = __syncthreads_or(bad ? 1 : 0) != 0;
-  const bool any_timeout = __syncthreads_or(timeout ? 1 : 0) != 0;
-  st_t = block_merge(st_t, sc, scratch);
-  if (info.pair) st_d = block_merge(st_d, sc, scratch);
+  uint64_t* parts = reinterpret_cast<uint64_t*>(P.parts);
+  const uint64_t tagw = static_cast<uint64_t>(P.tag) << 32;
 
-  // ---- exchange the CTA records through distributed shared memory
-  if (tid == 0) {
-    float* my = scratch + 32;  // staging of this CTA's record
-    my[R_MT] = st_t.m; my[R_ST] = st_t.s; my[R_IT] = __int_as_float(st_t.i);
-    my[R_MD] = st_d.m; my[R_SD] = st_d.s; my[R_ID] = __int_as_float(st_d.i);
-    const bool hasx = info.pair && info.tokok && info.x >= s_t.v0 && info.x < s_t.v0 + s_t.len;
-    my[R_XT] = hasx ? slice_elem<ES>(buf_t, s_t, info.x - s_t.v0) : 0.f;
-    my[R_XD] = hasx ? slice_elem<ES>(buf_d, s_d, info.x - s_d.v0) : 0.f;
-    my[R_HASX] = hasx ? 1.f : 0.f;
-    my[R_BAD] = __int_as_float((any_bad ? SV_DEVERR_NAN : 0) | (any_timeout ? SV_DEVERR_TIMEOUT : 0));
+  // ---- set-up: row_offsets into shared memory (when they fit), barriers,
+  //      the first NS units in flight
+  int32_t* offs_sm = reinterpret_cast<int32_t*>(smem_raw + kRowsHdrBytes + NS * 2 * P.rowbuf);
+  const int32_t* offs = P.offs;
+  if (P.offs_smem) {
+    for (int32_t i = tid; i <= P.B; i += blockDim.x) offs_sm[i] = __ldg(P.offs + i);
+    offs = offs_sm;
   }
   __syncthreads();
-  cluster_wait_acquire();  // every CTA of the cluster has started
-  if (tid < static_cast<int>(csize) * kRecWords) {
-    const int dst = tid / kRecWords, w = tid % kRecWords;
-    const float* my = scratch + 32;
-    const uint32_t a = smem_addr(recs + rank * kRecWords + w);
-    st_cluster_u32(mapa(a, dst), __float_as_uint(w <= R_BAD ? my[w] : 0.f));
+  if (warp == W_PROD && lane == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(sm.full(s), 2);                 // bulk-copy arm + cp.async completion
+      mbar_init(sm.empty(s), NCW + 2);          // consumers + publisher + gatherer
+      mbar_init(sm.partbar(s), NCW);
+      mbar_init(sm.statsbar(s), 1);
+    }
+    fence_mbar_init();
+    for (int i = 0; i < NS && i < n_units; ++i) produce_unit<ES>(P, sm, offs, c + i * N, i);
   }
-  cluster_arrive_release();
-  cluster_wait_acquire();
+  __syncthreads();
 
-  // ---- merge the C records in rank order (identical in every thread)
-  Stat gt = stat_empty(), gdr = stat_empty();
-  float xt = 0.f, xd = 0.f;
-  int flags = 0;
-  for (uint32_t q = 0; q < csize; ++q) {
-    const float* rq = recs + q * kRecWords;
-    gt = stat_merge(gt, Stat{rq[R_MT], rq[R_ST], __float_as_int(rq[R_IT])}, sc);
-    gdr = stat_merge(gdr, Stat{rq[R_MD], rq[R_SD], __float_as_int(rq[R_ID])}, sc);
-    if (rq[R_HASX] != 0.f) { xt = rq[R_XT]; xd = rq[R_XD]; }
-    flags |= __float_as_int(rq[R_BAD]);
-  }
-  if (!(gt.m > -INFINITY && gt.m < INFINITY)) flags |= SV_DEVERR_NAN;
-  if (info.pair && !(gdr.m > -INFINITY && gdr.m < INFINITY)) flags |= SV_DEVERR_NAN;
-  if (NEED_Z && !(gt.s > 0.f && gt.s < INFINITY)) flags |= SV_DEVERR_NAN;
-  if (NEED_Z && info.pair && !(gdr.s > 0.f && gdr.s < INFINITY)) flags |= SV_DEVERR_NAN;
-
-  // ---- pass 2: label c* over the resident slice pair
-  float conf = 0.f;
-  if (NEED_CONF && info.pair) {
-    const float lt = fmaf(gt.m, sc, __log2f(gt.s));
-    const float ld = fmaf(gdr.m, sc, __log2f(gdr.s));
-    float part = overlap_range<ES>(buf_t, s_t, buf_d, s_d, sc, lt, ld);
-    part = block_sum(part, scratch);
-    if (tid == 0) st_cluster_u32(mapa(smem_addr(cpart + rank), 0), __float_as_uint(part));
-    cluster_arrive_release();
-    cluster_wait_acquire();
-    if (rank == 0 && tid == 0)
-      for (uint32_t q = 0; q < csize; ++q) conf += cpart[q];
-  }
-
-  // ---- epilogue in CTA 0
-  if (rank == 0 && tid == 0) {
-    if (!info.ok) flags |= SV_DEVERR_LEN;
-    if (info.pair && !info.tokok) flags |= SV_DEVERR_TOKEN;
-    int acc = 0;
-    if (info.pair && info.tokok) {
-      if (P.mode == SV_GREEDY) {
-        acc = info.x == gt.i;
-      } else {
-        // ratio p_t(x) / p_d(x) = exp2(((xt - mt) - (xd - md)) * sc) * zd / zt
-        const float delta = (xt - gt.m) - (xd - gdr.m);
-        const float ratio = exp2f(delta * sc) * (gdr.s / gt.s);
-        const float u = __ldg(P.uniforms + g);
-        acc = u < ratio;
+  bool timeout = false;
+  if (warp < NCW) {
+    // =============================== consumer warps
+    const int ct = tid;
+    for (int32_t i = 0; i < n_units + kDelay; ++i) {
+      if (i < n_units) {  // pass 1 of unit i
+        const int s = i % NS;
+        mbar_wait(sm.full(s), (i / NS) & 1, timeout);
+        const RowInfo info = *sm.info(s);
+        bool bad = false;
+        const Slice s_t = target_slice<ES>(P, info);
+        const Slice s_d = draft_slice<ES>(P, info);
+        RStat a_t, a_d;
+        const bool fast = !TRACK && NEED_Z && info.pair && slice_aligned<ES>(s_t) &&
+                          slice_aligned<ES>(s_d) &&
+                          pass1_pair_fast<ES, NCT>(sm.tbuf(s), sm.dbuf(s), s_t.nbytes >> 4, sc, ct,
+                                                   a_t, a_d);
+        if (!fast) {
+          a_t = pass1_thread<ES, NCT, NEED_Z, TRACK>(sm.tbuf(s), s_t, sc, ct, bad);
+          a_d = info.pair ? pass1_thread<ES, NCT, NEED_Z, TRACK>(sm.dbuf(s), s_d, sc, ct, bad)
+                          : rstat_empty();
+        }
+        a_t = rstat_warp_reduce(a_t);
+        a_d = rstat_warp_reduce(a_d);
+        const unsigned badw = __ballot_sync(0xffffffffu, bad);
+        if (lane == 0) {
+          float* w = sm.part(s, warp);
+          w[R_HT] = a_t.h; w[R_ST] = a_t.s; w[R_MT] = a_t.m; w[R_IT] = __int_as_float(a_t.i);
+          w[R_HD] = a_d.h; w[R_SD] = a_d.s; w[R_MD] = a_d.m; w[R_ID] = __int_as_float(a_d.i);
+          w[R_BAD] = __int_as_float((badw ? SV_DEVERR_NAN : 0) | (timeout ? SV_DEVERR_TIMEOUT : 0));
+          mbar_arrive(sm.partbar(s));
+        }
+      }
+      if (i >= kDelay) {  // pass 2 of unit j = i - kDelay, then release its stage
+        const int32_t j = i - kDelay;
+        const int s = j % NS;
+        const RowInfo info = *sm.info(s);
+        if (NEED_CONF && info.pair) {
+          mbar_wait(sm.statsbar(s), (j / NS) & 1, timeout);
+          const float* st = sm.stats(s);
+          float part = pass2_thread<ES, NCT>(sm.tbuf(s), target_slice<ES>(P, info), sm.dbuf(s),
+                                             draft_slice<ES>(P, info), sc, st[0], st[4], st[6],
+                                             ct);
+          part = warp_sum_f32(part);
+          if (lane == 0) sm.cp(s)[warp] = part;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sm.empty(s));
       }
     }
-    RowRec rr;
-    rr.mt = gt.m; rr.zt = gt.s; rr.md = gdr.m; rr.zd = gdr.s;
-    rr.argt = gt.i; rr.acc = acc; rr.pick = -1; rr.flags = flags;
-    P.rec[g] = rr;
-    if (NEED_CONF && info.pair && P.out_conf != nullptr) P.out_conf[info.gd] = conf;
-    if (P.out_row_stats != nullptr) {
-      float* o = P.out_row_stats + 3 * static_cast<size_t>(g);
-      o[0] = gt.m / P.T; o[1] = gt.s; o[2] = __int_as_float(gt.i);
-      if (info.pair) {
-        float* q = P.out_row_stats + 3 * (static_cast<size_t>(P.Nt) + info.gd);
-        q[0] = gdr.m / P.T; q[1] = gdr.s; q[2] = __int_as_float(gdr.i);
+  } else if (warp == W_PROD) {
+    // =============================== producer warp
+    for (int32_t j = 0; j < n_units; ++j) {
+      const int s = j % NS;
+      mbar_wait(sm.empty(s), (j / NS) & 1, timeout);
+      if (lane == 0) {
+        const RowInfo pj = *sm.info(s);
+        if (NEED_CONF && pj.pair) {  // label partial of unit j
+          float cs = 0.f;
+          for (int w = 0; w < NCW; ++w) cs += sm.cp(s)[w];
+          P.cpart[static_cast<size_t>(pj.g) * kMaxSlices + pj.k] = cs / sm.stats(s)[1];
+        }
+        if (j + NS < n_units) produce_unit<ES>(P, sm, offs, c + (j + NS) * N, s);
       }
+      __syncwarp();
     }
-    if (flags) raise_error(P, flags);
+  } else if (warp < W_GATH) {
+    // =============================== publisher warps (unit i by warp i % kPublishers)
+    for (int32_t i = warp - W_PUB; i < n_units; i += kPublishers) {
+      const int s = i % NS;
+      mbar_wait(sm.partbar(s), (i / NS) & 1, timeout);
+      mbar_wait(sm.full(s), (i / NS) & 1, timeout);
+      const RowInfo info = *sm.info(s);
+      RStat b_t = rstat_empty(), b_d = rstat_empty();
+      int flags = 0;
+      if (lane < NCW) {
+        const float* w = sm.part(s, lane);
+        b_t = RStat{w[R_HT], w[R_ST], w[R_MT], __float_as_int(w[R_IT])};
+        b_d = RStat{w[R_HD], w[R_SD], w[R_MD], __float_as_int(w[R_ID])};
+        flags = __float_as_int(w[R_BAD]);
+      }
+      b_t = rstat_warp_reduce(b_t);
+      b_d = rstat_warp_reduce(b_d);
+      flags = __reduce_or_sync(0xffffffffu, flags);
+      const Slice s_t = target_slice<ES>(P, info);
+      const bool hasx = info.pair && info.x >= s_t.v0 && info.x < s_t.v0 + s_t.len;
+      float xt = 0.f, xd = 0.f;
+      if (hasx) {
+        xt = slice_elem<ES>(sm.tbuf(s), s_t, info.x - s_t.v0);
+        xd = slice_elem<ES>(sm.dbuf(s), draft_slice<ES>(P, info), info.x - s_t.v0);
+      }
+      // lane w < R_NWORDS publishes word w of the partial, tagged
+      uint32_t word = 0;
+      switch (lane) {
+        case R_HT: word = __float_as_uint(b_t.h); break;
+        case R_ST: word = __float_as_uint(b_t.s); break;
+        case R_MT: word = __float_as_uint(b_t.m); break;
+        case R_IT: word = static_cast<uint32_t>(b_t.i); break;
+        case R_HD: word = __float_as_uint(b_d.h); break;
+        case R_SD: word = __float_as_uint(b_d.s); break;
+        case R_MD: word = __float_as_uint(b_d.m); break;
+        case R_ID: word = static_cast<uint32_t>(b_d.i); break;
+        case R_BAD: word = static_cast<uint32_t>(flags); break;
+        case R_XT: word = __float_as_uint(xt); break;
+        case R_XD: word = __float_as_uint(xd); break;
+        case R_HASX: word = hasx ? 1u : 0u; break;
+        default: break;
+      }
+      if (lane < R_NWORDS) {
+        uint64_t* dst = parts + (static_cast<size_t>(info.g) * kMaxSlices + info.k) * kPartWords;
+        st_relaxed_u64(dst + lane, tagw | word);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.empty(s));
+    }
+  } else {
+    // =============================== gatherer warps (unit j by warp j % kGatherers)
+    const int q = warp - W_GATH;
+    for (int32_t j = q; j < n_units; j += kGatherers) {
+      const int s = j % NS;
+      mbar_wait(sm.full(s), (j / NS) & 1, timeout);
+      const RowInfo info = *sm.info(s);
+      // start polling once this CTA has finished pass 1 of the unit (the
+      // other slices of the row are handled in the same round elsewhere)
+      mbar_wait(sm.partbar(s), (j / NS) & 1, timeout);
+      // wait until the S partials of this row carry this call's tag (lane =
+      // slice): poll one word per slice, then read all words and check each
+      const uint64_t* row_parts = parts + static_cast<size_t>(info.g) * kMaxSlices * kPartWords;
+      const bool mine = lane < P.nslices;
+      const uint64_t* src = row_parts + (mine ? lane : 0) * kPartWords;
+      uint32_t wv[R_NWORDS];
+      auto full_read = [&]() {
+        bool ok = true;
+        if (mine) {
+#pragma unroll
+          for (int w = 0; w < R_NWORDS; ++w) {
+            const uint64_t v = ld_relaxed_u64(src + w);
+            wv[w] = static_cast<uint32_t>(v);
+            ok &= (v & 0xffffffff00000000ull) == tagw;
+          }
+        }
+        return ok;
+      };
+      bool done = false;
+      const uint64_t t0 = globaltimer_ns();
+      for (uint32_t n = 0; !done; ++n) {
+        const bool seen = !mine || (ld_relaxed_u64(src + R_BAD) & 0xffffffff00000000ull) == tagw;
+        if (__all_sync(0xffffffffu, seen)) done = __all_sync(0xffffffffu, full_read());
+        if (!done) {
+          if (timeout || globaltimer_ns() - t0 > kWaitLimitNs) {
+            timeout = true;
+            break;
+          }
+          __nanosleep(256);
+        }
+      }
+      RStat gt = rstat_empty(), gdr = rstat_empty();
+      int flags = 0;
+      float xt = 0.f, xd = 0.f;
+      bool hasx = false;
+      if (mine) {
+        gt = RStat{__uint_as_float(wv[R_HT]), __uint_as_float(wv[R_ST]), __uint_as_float(wv[R_MT]),
+                   static_cast<int32_t>(wv[R_IT])};
+        gdr = RStat{__uint_as_float(wv[R_HD]), __uint_as_float(wv[R_SD]),
+                    __uint_as_float(wv[R_MD]), static_cast<int32_t>(wv[R_ID])};
+        flags = static_cast<int>(wv[R_BAD]);
+        xt = __uint_as_float(wv[R_XT]);
+        xd = __uint_as_float(wv[R_XD]);
+        hasx = wv[R_HASX] != 0;
+      }
+      gt = rstat_warp_reduce(gt);
+      gdr = rstat_warp_reduce(gdr);
+      flags = __reduce_or_sync(0xffffffffu, flags) | (timeout ? SV_DEVERR_TIMEOUT : 0);
+      const unsigned xl = __ballot_sync(0xffffffffu, hasx);
+      if (xl) {
+        xt = __shfl_sync(0xffffffffu, xt, __ffs(xl) - 1);
+        xd = __shfl_sync(0xffffffffu, xd, __ffs(xl) - 1);
+      }
+      if (lane == 0) {
+        float* st = sm.stats(s);
+        st[0] = gt.h;
+        st[1] = gt.s;
+        st[4] = gdr.h;
+        st[5] = gdr.s;
+        st[6] = __log2f(gdr.s) - __log2f(gt.s);  // delta of pass 2
+        mbar_arrive(sm.statsbar(s));
+      }
+      if (info.k == 0 && lane == 0) {  // row epilogue, once per row
+        const int32_t g = info.g, ell = info.ell;
+        const bool ok = info.off <= g && g < info.off1 && info.off1 - info.off == ell && ell >= 1 &&
+                        ell <= P.max_len && info.off >= info.r;
+        const bool tokok = info.x >= 0 && info.x < P.V;
+        int fl = flags;
+        if (NEED_Z && !(gt.s > 0.f && gt.s < INFINITY)) fl |= SV_DEVERR_NAN;
+        if (NEED_Z && info.pair && !(gdr.s > 0.f && gdr.s < INFINITY)) fl |= SV_DEVERR_NAN;
+        if (TRACK && !(gt.m > -INFINITY && gt.m < INFINITY)) fl |= SV_DEVERR_NAN;
+        if (TRACK && info.pair && !(gdr.m > -INFINITY && gdr.m < INFINITY)) fl |= SV_DEVERR_NAN;
+        if (!ok) fl |= SV_DEVERR_LEN;
+        if (info.pair && !tokok) fl |= SV_DEVERR_TOKEN;
+        int acc = 0;
+        if (ok && info.pair && tokok) {
+          if (P.mode == SV_GREEDY) {
+            acc = info.x == gt.i;
+          } else {
+            // p_t(x) / p_d(x) = 2^(a - b) * s_d / s_t, a = x_t sc - h_t, b = x_d sc - h_d
+            const float ratio =
+                exp2f(fmaf(xt, sc, -gt.h) - fmaf(xd, sc, -gdr.h)) * (gdr.s / gt.s);
+            acc = info.u < ratio;
+          }
+        }
+        RowRec rr;
+        rr.mt = gt.h; rr.zt = gt.s; rr.md = gdr.h; rr.zd = gdr.s;
+        rr.argt = gt.i; rr.acc = acc; rr.pick = -1; rr.flags = fl;
+        P.rec[g] = rr;
+        if (TRACK && P.out_row_stats != nullptr) {
+          // Z relative to the true max: s * 2^(h - m sc)
+          float* o = P.out_row_stats + 3 * static_cast<size_t>(g);
+          o[0] = gt.m / P.T;
+          o[1] = gt.s * exp2f(-fmaf(gt.m, sc, -gt.h));
+          o[2] = __int_as_float(gt.i);
+          if (info.pair) {
+            float* o2 = P.out_row_stats + 3 * (static_cast<size_t>(P.Nt) + info.gd);
+            o2[0] = gdr.m / P.T;
+            o2[1] = gdr.s * exp2f(-fmaf(gdr.m, sc, -gdr.h));
+            o2[2] = __int_as_float(gdr.i);
+          }
+        }
+        if (fl) raise_error(P, fl);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sm.empty(s));
+    }
   }
-
-  if (any_timeout) {  // never leave while a copy into this CTA may still land
-    for (int c = 0; c < kChunks; ++c) mbar_wait_bounded(bar0 + 8 * c, 0, kSpinLimit);
-  }
+  if (timeout && lane == 0) raise_error(P, SV_DEVERR_TIMEOUT);
 }
 
 }  // namespace sv

@@ -30,7 +30,7 @@ def oracle_requests(w, requests, *, mode, temperature, top_k, top_p, want_conf=T
         d = oracle.decode_logits(workloads.bits_of(w.draft[doff:doff + ell - 1]), dt)
         x = w.draft_tokens[doff:doff + ell - 1].cpu().numpy()
         u = w.uniforms[off:off + ell].double().cpu().numpy()
-        res[r] = oracle.verify_request(t, d.reshape(ell - 1, -1), x, u, temperature, top_k,
+        res[r] = oracle.verify_request(t, d.reshape(ell - 1, t.shape[1]), x, u, temperature, top_k,
                                        top_p, mode, want_conf=want_conf)
     return res
 

@@ -18,19 +18,21 @@ DEV = "cuda:0"
 
 
 @contextmanager
-def cluster_size(c):
-    old = os.environ.get("SPEC_VERIFY_CLUSTER")
-    if c is None:
-        os.environ.pop("SPEC_VERIFY_CLUSTER", None)
+def slice_len(L):
+    """Force the rows kernel's slice length (elements): several slices per
+    row exercise the cross-CTA exchange even at small V."""
+    old = os.environ.get("SPEC_VERIFY_SLICE")
+    if L is None:
+        os.environ.pop("SPEC_VERIFY_SLICE", None)
     else:
-        os.environ["SPEC_VERIFY_CLUSTER"] = str(c)
+        os.environ["SPEC_VERIFY_SLICE"] = str(L)
     try:
         yield
     finally:
         if old is None:
-            os.environ.pop("SPEC_VERIFY_CLUSTER", None)
+            os.environ.pop("SPEC_VERIFY_SLICE", None)
         else:
-            os.environ["SPEC_VERIFY_CLUSTER"] = old
+            os.environ["SPEC_VERIFY_SLICE"] = old
 
 
 def run_and_compare(cuda_lib, w, *, requests=None, T=None, top_k=None, top_p=None,
@@ -53,23 +55,24 @@ def run_and_compare(cuda_lib, w, *, requests=None, T=None, top_k=None, top_p=Non
 
 
 SMALL = [
-    # (workload index, V, B, lens, forced cluster)
+    # (workload index, V, B, lens, forced slice length)
     (0, None, None, None, None),
-    (1, 20000, None, None, 1),
-    (1, 20000, None, None, 4),
-    (1, 20000, None, None, 16),
-    (2, 8191, 6, None, 8),          # odd V: rows not 16-byte aligned
-    (2, 4099, 5, None, 3),          # cluster size that is not a power of two
-    (3, 5003, 40, None, 4),         # ragged lengths
-    (3, 777, None, [1, 16, 2, 1, 9], 2),
+    (0, None, None, None, 96),      # fp32 rows of 1000 in 11 slices
+    (1, 20000, None, None, None),
+    (1, 20000, None, None, 1000),   # 20 slices per row
+    (1, 20000, None, None, 640),    # 32 slices per row (the maximum)
+    (2, 8191, 6, None, 512),        # odd V: rows not 16-byte aligned
+    (2, 4099, 5, None, 1368),       # 3 slices, short last slice
+    (3, 5003, 40, None, 800),       # ragged lengths
+    (3, 777, None, [1, 16, 2, 1, 9], 200),
 ]
 
 
 @pytest.mark.parametrize("mode", [W.SAMPLE, W.GREEDY])
-@pytest.mark.parametrize("idx,V,B,lens,C", SMALL)
-def test_small_workloads_every_request(cuda_lib, idx, V, B, lens, C, mode):
+@pytest.mark.parametrize("idx,V,B,lens,L", SMALL)
+def test_small_workloads_every_request(cuda_lib, idx, V, B, lens, L, mode):
     w = W.make_workload(W.WORKLOADS[idx], mode, seed=7 + idx, device=DEV, B=B, V=V, lens=lens)
-    with cluster_size(C):
+    with slice_len(L):
         run_and_compare(cuda_lib, w)
 
 
@@ -216,11 +219,11 @@ def test_host_errors_through_binding(cuda_lib):
         cuda_lib.verify_workload(w, max_len=0)
 
 
-def test_deterministic_across_runs_and_cluster_sizes(cuda_lib):
+def test_deterministic_across_runs_and_slice_lengths(cuda_lib):
     w = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=13, device=DEV, B=8, V=40000)
     first = None
-    for C in (None, None, 1, 2, 4, 8, 16):
-        with cluster_size(C):
+    for L in (None, None, 13000, 10000, 2504, 1256):
+        with slice_len(L):
             out = cuda_lib.verify_workload(w, want_stats=True)
         torch.cuda.synchronize()
         cur = (out.tokens.cpu().numpy(), out.accept_len.cpu().numpy(), out.conf.cpu().numpy(),
@@ -228,7 +231,7 @@ def test_deterministic_across_runs_and_cluster_sizes(cuda_lib):
         if first is None:
             first = cur
             continue
-        if C is None:  # same configuration: bitwise identical
+        if L is None:  # same configuration: bitwise identical
             for a, b in zip(first, cur):
                 assert np.array_equal(a, b)
         else:
