@@ -65,25 +65,27 @@ bool is_filtered(int V, int top_k, float top_p) {
 }
 
 // Geometry of the rows kernel: a row is cut into S <= kMaxSlices slices of
-// L elements (L a multiple of the 16-byte vector, about 8192 bf16 / 4096
-// fp32 elements by default: SPEC_VERIFY_SLICE overrides); as many stages
-// (kDelay + 2 .. kMaxStages) as the shared memory allows.
+// L elements (L a multiple of the 16-byte vector; about 13000 bf16 / 6500
+// fp32 elements by default, SPEC_VERIFY_SLICE overrides) and as many stages
+// (kMinStages .. kMaxStages, SPEC_VERIFY_STAGES caps) as the shared memory
+// allows next to the row_offsets copy (B + 1 entries when they fit).
 struct RowsGeom {
-  int L, S, stages, smem;
+  int L, S, stages, smem, offs_smem;
 };
 
-int rows_geometry(int V, int es, const DeviceCache& dc, RowsGeom* g) {
+int rows_geometry(int V, int B, int es, const DeviceCache& dc, RowsGeom* g) {
   const int vec = 16 / es;
-  const int target = env_int("SPEC_VERIFY_SLICE", 16384 / es);
+  const int target = env_int("SPEC_VERIFY_SLICE", 26000 / es);
   int S = std::max(1, (V + target - 1) / target);
   S = std::min(S, kMaxSlices);
-  int L = round_up((V + S - 1) / S, vec);
+  const int L = round_up((V + S - 1) / S, vec);
   S = (V + L - 1) / L;  // no empty trailing slice
+  const int offs = B + 1 <= kMaxSmemOffsets ? round_up((B + 1) * 4, 128) : 0;
   const int max_stages = std::min(kMaxStages, env_int("SPEC_VERIFY_STAGES", kMaxStages));
-  for (int ns = max_stages; ns >= kDelay + 2; --ns) {
-    const int smem = kRowsHdrBytes + ns * 2 * rowbuf_bytes(L, es);
-    if (smem + kMaxSmemOffsets * 4 <= dc.max_smem_optin) {
-      *g = RowsGeom{L, S, ns, smem};
+  for (int ns = max_stages; ns >= kMinStages; --ns) {
+    const int smem = kRowsHdrBytes + ns * 2 * rowbuf_bytes(L, es) + offs;
+    if (smem <= dc.max_smem_optin) {
+      *g = RowsGeom{L, S, ns, smem, offs > 0};
       return SV_OK;
     }
   }
@@ -340,7 +342,7 @@ int run_rows(const Args& a) {
   Params P = make_params(a);
   const int es = a.dtype == SV_BF16 ? 2 : 4;
   RowsGeom geo;
-  rc = rows_geometry(a.V, es, dc, &geo);
+  rc = rows_geometry(a.V, a.B, es, dc, &geo);
   if (rc != SV_OK) return rc;
   P.S = geo.L;
   P.nslices = geo.S;
@@ -348,9 +350,8 @@ int run_rows(const Args& a) {
   P.rowbuf = rowbuf_bytes(geo.L, es);
   P.nstages = geo.stages;
   P.tag = next_tag();
-  P.offs_smem = a.B + 1 <= kMaxSmemOffsets;
-  const int smem = geo.smem + (P.offs_smem ? round_up((a.B + 1) * 4, 128) : 0);
-  if (smem > dc.max_smem_optin) return SV_ERR_UNSUPPORTED;
+  P.offs_smem = geo.offs_smem;
+  const int smem = geo.smem;
   // z is needed for sampling, labels and statistics; the exact max / argmax
   // only for greedy decisions and statistics
   const bool need_z = a.mode == SV_SAMPLE || a.out_conf != nullptr || a.out_row_stats != nullptr;
@@ -372,7 +373,7 @@ int run_finalize(const Args& a) {
   Params P = make_params(a);
   const int es = a.dtype == SV_BF16 ? 2 : 4;
   RowsGeom geo;
-  rc = rows_geometry(a.V, es, dc, &geo);
+  rc = rows_geometry(a.V, a.B, es, dc, &geo);
   if (rc != SV_OK) return rc;
   P.nslices = geo.S;
   cudaStream_t st = static_cast<cudaStream_t>(a.stream);
@@ -460,7 +461,7 @@ int spec_verify_slices_per_row(int32_t V, int32_t dtype, int32_t top_k, float to
   const int rc = sv::device_info(&dc);
   if (rc != SV_OK) return rc;
   sv::RowsGeom geo;
-  const int g = sv::rows_geometry(V, dtype == SV_BF16 ? 2 : 4, dc, &geo);
+  const int g = sv::rows_geometry(V, 1, dtype == SV_BF16 ? 2 : 4, dc, &geo);
   return g != SV_OK ? g : geo.S;
 }
 

@@ -16,7 +16,9 @@
 // itself: no release/acquire pair, one L2 round trip per poll.
 //
 // Warp roles (mbarriers between them; no CTA-wide barrier in the loop):
-//  * NCW consumer warps: pass 1 of unit i, then pass 2 of unit i - kDelay;
+//  * NCW consumer warps in two groups (labels on): one runs pass 1 of the
+//    units, the other pass 2, each on its own stream of units, so that the
+//    exchange of a unit's statistics overlaps pass 1 of later units;
 //  * producer warp: refills a stage once every role has released it (row
 //    metadata arrives by cp.async on the stage's `full` mbarrier) and writes
 //    the unit's label partial;
@@ -54,10 +56,17 @@
 namespace sv {
 
 constexpr int kMaxStages = 6;
-constexpr int kDelay = 3;             // pass 2 of unit i - kDelay follows pass 1 of unit i
+// An mbarrier parity wait cannot tell "my phase completed" from "the barrier
+// is still one phase behind me", so no warp may wait on a stage's barrier
+// before the previous use of that stage has passed the same barrier.  Warps
+// that handle every unit wait in order; a gatherer handles every kGatherers-th
+// unit and a publisher every kPublishers-th, so their previous unit implies
+// the stage's previous use is done only when stages >= both counts.
+constexpr int kMinStages = 4;
 constexpr int kMaxConsumerWarps = 16;
 constexpr int kPublishers = 2;
 constexpr int kGatherers = 4;
+static_assert(kMinStages >= kGatherers && kMinStages >= kPublishers, "stage reuse order");
 constexpr int kMaxSlices = 32;        // slices per row (gatherer lanes)
 constexpr int kPartWords = 16;        // 64-bit words per published partial (12 used)
 constexpr int kMaxSmemOffsets = 4096; // row_offsets entries kept in shared memory
@@ -205,82 +214,125 @@ __device__ __forceinline__ RStat pass1_thread(const unsigned char* buf, const Sl
   return st;
 }
 
-// Pass 1 fast path for a slice pair on one vector grid with no masked lanes
-// and no need for the exact max: both rows in one loop, the references taken
-// from the thread's first vector of each row.  Returns false (the caller then
-// runs the general path) on a non-finite input or an overflow.
-template <int ES, int NCT>
+// sum_l exp2(x_l * sc - h) over one vector, as a packed pair of partial sums
+// (fma / add on float2: two lanes per instruction on sm_100+).
+template <int VEC>
+__device__ __forceinline__ float2 sum_exp2_x2(const float* x, float2 sc2, float2 nh2) {
+  float e[VEC];
+#pragma unroll
+  for (int l = 0; l < VEC; l += 2) {
+    const float2 a = __ffma2_rn(make_float2(x[l], x[l + 1]), sc2, nh2);
+    e[l] = ex2(a.x);
+    e[l + 1] = ex2(a.y);
+  }
+  float2 acc = make_float2(e[0], e[1]);
+#pragma unroll
+  for (int l = 2; l < VEC; l += 2) acc = __fadd2_rn(acc, make_float2(e[l], e[l + 1]));
+  return acc;
+}
+
+// Pass 1 fast path of one warp of the pass-1 group for a slice pair with no
+// masked lanes, when the exact max is not needed: both rows in one loop,
+// every lane of the warp using the same references (the warp maximum of the
+// lanes' first vectors), so the warp's partials are plain sums.  Returns
+// false, uniformly over the warp, on a non-finite input or an overflow (the
+// caller then runs the general path).
+template <int ES, int NT1>
 __device__ __forceinline__ bool pass1_pair_fast(const unsigned char* bt, const unsigned char* bd,
                                                 int32_t nv, float sc, int ct, RStat& at,
                                                 RStat& ad) {
   constexpr int VEC = 16 / ES;
-  at = rstat_empty();
-  ad = rstat_empty();
-  int32_t k = ct;
-  if (k >= nv) return true;
   float t[VEC], d[VEC];
-  load_vec_raw<ES>(bt, k, t);
-  load_vec_raw<ES>(bd, k, d);
-  const float mt = vmax_nan<VEC>(t), md = vmax_nan<VEC>(d);
-  if (!(mt > -INFINITY && mt < INFINITY && md > -INFINITY && md < INFINITY)) return false;
-  const float ht = mt * sc, hd = md * sc;
-  float st = sum_exp2<VEC>(t, sc, ht), sd = sum_exp2<VEC>(d, sc, hd);
-#pragma unroll 2
-  for (k += NCT; k < nv; k += NCT) {
+  float mt = -INFINITY, md = -INFINITY;
+  int32_t k = ct;
+  if (k < nv) {
     load_vec_raw<ES>(bt, k, t);
     load_vec_raw<ES>(bd, k, d);
-    st += sum_exp2<VEC>(t, sc, ht);
-    sd += sum_exp2<VEC>(d, sc, hd);
+    mt = vmax_nan<VEC>(t);
+    md = vmax_nan<VEC>(d);
   }
-  if (!(st < INFINITY && sd < INFINITY)) return false;
+  // NaN or +inf in a first vector: general path for the whole warp
+  if (!__all_sync(0xffffffffu, !(mt != mt || md != md || mt == INFINITY || md == INFINITY)))
+    return false;
+  const float ht = warp_max_f32(mt) * sc, hd = warp_max_f32(md) * sc;
+  const float2 sc2 = make_float2(sc, sc), nht = make_float2(-ht, -ht),
+               nhd = make_float2(-hd, -hd);
+  float2 at2 = make_float2(0.f, 0.f), ad2 = make_float2(0.f, 0.f);
+  if (k < nv) {
+    at2 = sum_exp2_x2<VEC>(t, sc2, nht);
+    ad2 = sum_exp2_x2<VEC>(d, sc2, nhd);
+#pragma unroll 2
+    for (k += NT1; k < nv; k += NT1) {
+      load_vec_raw<ES>(bt, k, t);
+      load_vec_raw<ES>(bd, k, d);
+      at2 = __fadd2_rn(at2, sum_exp2_x2<VEC>(t, sc2, nht));
+      ad2 = __fadd2_rn(ad2, sum_exp2_x2<VEC>(d, sc2, nhd));
+    }
+  }
+  float st = at2.x + at2.y, sd = ad2.x + ad2.y;
+  if (!__all_sync(0xffffffffu, st < INFINITY && sd < INFINITY)) return false;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {  // two independent shuffle chains
+    st += __shfl_xor_sync(0xffffffffu, st, off);
+    sd += __shfl_xor_sync(0xffffffffu, sd, off);
+  }
   at = RStat{ht, st, -INFINITY, 0x7fffffff};
   ad = RStat{hd, sd, -INFINITY, 0x7fffffff};
   return true;
 }
 
-// Pass 2 of one consumer thread: sum of exp2(min(a, b - delta)) over its vectors.
-template <int ES, int NCT>
+// Pass 2 of one thread of the pass-2 group: sum of exp2(min(a, b)) over its
+// vectors, a = t sc - h_t, b = d sc - k_d with k_d = h_d + delta.  kd_hi +
+// kd_lo represents k_d exactly; when kd_lo is 0 (FOLD) the subtraction
+// disappears (the caller folds only when that costs at most ~2e-6 in c*).
+template <int ES, int NT2, bool FOLD>
+__device__ __forceinline__ float pass2_aligned(const unsigned char* bt, const unsigned char* bd,
+                                               int32_t nv, float sc, float ht, float kd_hi,
+                                               float kd_lo, int ct) {
+  constexpr int VEC = 16 / ES;
+  const float2 sc2 = make_float2(sc, sc), nht = make_float2(-ht, -ht),
+               nkd = make_float2(-kd_hi, -kd_hi), nlo = make_float2(-kd_lo, -kd_lo);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll 2
+  for (int32_t k = ct; k < nv; k += NT2) {
+    float t[VEC], d[VEC];
+    load_vec_raw<ES>(bt, k, t);
+    load_vec_raw<ES>(bd, k, d);
+    float e[VEC];
+#pragma unroll
+    for (int l = 0; l < VEC; l += 2) {
+      const float2 a = __ffma2_rn(make_float2(t[l], t[l + 1]), sc2, nht);
+      float2 b = __ffma2_rn(make_float2(d[l], d[l + 1]), sc2, nkd);
+      if (!FOLD) b = __fadd2_rn(b, nlo);
+      e[l] = ex2(fminf(a.x, b.x));
+      e[l + 1] = ex2(fminf(a.y, b.y));
+    }
+#pragma unroll
+    for (int l = 0; l < VEC; l += 2) acc = __fadd2_rn(acc, make_float2(e[l], e[l + 1]));
+  }
+  return acc.x + acc.y;
+}
+
+// Pass 2, general path (slices with masked ends or different 16-byte phases):
+// sum of exp2(min(a, b - delta)) over the thread's elements.
+template <int ES, int NT2>
 __device__ __forceinline__ float pass2_thread(const unsigned char* bt, const Slice& st_,
                                               const unsigned char* bd, const Slice& sd_, float sc,
                                               float ht, float hd, float delta, int ct) {
   constexpr int VEC = 16 / ES;
   float acc = 0.f;
-  if (slice_aligned<ES>(st_) && slice_aligned<ES>(sd_)) {  // no masked lanes
+  if (st_.hoff == sd_.hoff) {  // same vector grid: vectorised, masked ends
     const int32_t nv = st_.nbytes >> 4;
-#pragma unroll 2
-    for (int32_t k = ct; k < nv; k += NCT) {
-      float t[VEC], d[VEC];
-      load_vec_raw<ES>(bt, k, t);
-      load_vec_raw<ES>(bd, k, d);
-      float e[VEC];
-#pragma unroll
-      for (int l = 0; l < VEC; ++l)
-        e[l] = ex2(fminf(fmaf(t[l], sc, -ht), fmaf(d[l], sc, -hd) - delta));
-#pragma unroll
-      for (int w = VEC / 2; w > 0; w >>= 1)
-#pragma unroll
-        for (int l = 0; l < w; ++l) e[l] += e[l + w];
-      acc += e[0];
-    }
-  } else if (st_.hoff == sd_.hoff) {  // same vector grid: vectorised, masked ends
-    const int32_t nv = st_.nbytes >> 4;
-#pragma unroll 2
-    for (int32_t k = ct; k < nv; k += NCT) {
+    for (int32_t k = ct; k < nv; k += NT2) {
       float t[VEC], d[VEC];
       load_vec<ES>(bt, st_, k, t);
       load_vec<ES>(bd, sd_, k, d);
-      float e[VEC];
 #pragma unroll
       for (int l = 0; l < VEC; ++l)
-        e[l] = ex2(fminf(fmaf(t[l], sc, -ht), fmaf(d[l], sc, -hd) - delta));
-#pragma unroll
-      for (int w = VEC / 2; w > 0; w >>= 1)
-#pragma unroll
-        for (int l = 0; l < w; ++l) e[l] += e[l + w];
-      acc += e[0];
+        acc += ex2(fminf(fmaf(t[l], sc, -ht), fmaf(d[l], sc, -hd) - delta));
     }
-  } else {  // rows with different 16-byte phase (V * esize not a multiple of 16)
-    for (int32_t i = ct; i < st_.len; i += NCT) {
+  } else {  // different 16-byte phases (V * esize not a multiple of 16)
+    for (int32_t i = ct; i < st_.len; i += NT2) {
       const float t = slice_elem<ES>(bt, st_, i), d = slice_elem<ES>(bd, sd_, i);
       acc += ex2(fminf(fmaf(t, sc, -ht), fmaf(d, sc, -hd) - delta));
     }
@@ -384,8 +436,10 @@ constexpr int rows_threads(int ncw) { return (ncw + 1 + kPublishers + kGatherers
 
 template <int ES, int NCW, bool NEED_Z, bool NEED_CONF, bool TRACK>
 __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params P) {
-  static_assert(NCW <= kMaxConsumerWarps, "consumer warps");
-  constexpr int NCT = NCW * 32;
+  static_assert(NCW <= kMaxConsumerWarps && NCW % 2 == 0, "consumer warps");
+  constexpr int NW1 = NEED_CONF ? NCW / 2 : NCW;  // pass-1 warps
+  constexpr int NW2 = NCW - NW1;                  // pass-2 warps
+  constexpr int NT1 = NW1 * 32, NT2 = NW2 > 0 ? NW2 * 32 : 32;
   constexpr int W_PROD = NCW, W_PUB = NCW + 1, W_GATH = NCW + 1 + kPublishers;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const RowsSmem sm{smem_raw, P.rowbuf};
@@ -410,8 +464,8 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
   if (warp == W_PROD && lane == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(sm.full(s), 2);                 // bulk-copy arm + cp.async completion
-      mbar_init(sm.empty(s), NCW + 2);          // consumers + publisher + gatherer
-      mbar_init(sm.partbar(s), NCW);
+      mbar_init(sm.empty(s), (NEED_CONF ? NW2 : NW1) + 2);  // + publisher + gatherer
+      mbar_init(sm.partbar(s), NW1);
       mbar_init(sm.statsbar(s), 1);
     }
     fence_mbar_init();
@@ -422,9 +476,11 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
   bool timeout = false;
   if (warp < NCW) {
     // =============================== consumer warps
-    const int ct = tid;
-    for (int32_t i = 0; i < n_units + kDelay; ++i) {
-      if (i < n_units) {  // pass 1 of unit i
+    // Labels on: warps [0, NW1) run pass 1, warps [NW1, NCW) pass 2, each
+    // group on its own stream of units.  Labels off: all run pass 1.
+    if (warp < NW1) {
+      const int ct = tid;
+      for (int32_t i = 0; i < n_units; ++i) {  // pass 1 of unit i
         const int s = i % NS;
         mbar_wait(sm.full(s), (i / NS) & 1, timeout);
         const RowInfo info = *sm.info(s);
@@ -434,15 +490,15 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         RStat a_t, a_d;
         const bool fast = !TRACK && NEED_Z && info.pair && slice_aligned<ES>(s_t) &&
                           slice_aligned<ES>(s_d) &&
-                          pass1_pair_fast<ES, NCT>(sm.tbuf(s), sm.dbuf(s), s_t.nbytes >> 4, sc, ct,
+                          pass1_pair_fast<ES, NT1>(sm.tbuf(s), sm.dbuf(s), s_t.nbytes >> 4, sc, ct,
                                                    a_t, a_d);
-        if (!fast) {
-          a_t = pass1_thread<ES, NCT, NEED_Z, TRACK>(sm.tbuf(s), s_t, sc, ct, bad);
-          a_d = info.pair ? pass1_thread<ES, NCT, NEED_Z, TRACK>(sm.dbuf(s), s_d, sc, ct, bad)
+        if (!fast) {  // general path: per-thread partials, then a warp merge
+          a_t = pass1_thread<ES, NT1, NEED_Z, TRACK>(sm.tbuf(s), s_t, sc, ct, bad);
+          a_d = info.pair ? pass1_thread<ES, NT1, NEED_Z, TRACK>(sm.dbuf(s), s_d, sc, ct, bad)
                           : rstat_empty();
+          a_t = rstat_warp_reduce(a_t);
+          a_d = rstat_warp_reduce(a_d);
         }
-        a_t = rstat_warp_reduce(a_t);
-        a_d = rstat_warp_reduce(a_d);
         const unsigned badw = __ballot_sync(0xffffffffu, bad);
         if (lane == 0) {
           float* w = sm.part(s, warp);
@@ -450,20 +506,38 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
           w[R_HD] = a_d.h; w[R_SD] = a_d.s; w[R_MD] = a_d.m; w[R_ID] = __int_as_float(a_d.i);
           w[R_BAD] = __int_as_float((badw ? SV_DEVERR_NAN : 0) | (timeout ? SV_DEVERR_TIMEOUT : 0));
           mbar_arrive(sm.partbar(s));
+          if (!NEED_CONF) mbar_arrive(sm.empty(s));  // no pass 2: release the stage
         }
       }
-      if (i >= kDelay) {  // pass 2 of unit j = i - kDelay, then release its stage
-        const int32_t j = i - kDelay;
+    } else {
+      const int ct = tid - NT1;
+      for (int32_t j = 0; j < n_units; ++j) {  // pass 2 of unit j, then release its stage
         const int s = j % NS;
+        mbar_wait(sm.full(s), (j / NS) & 1, timeout);
         const RowInfo info = *sm.info(s);
-        if (NEED_CONF && info.pair) {
+        if (info.pair) {
           mbar_wait(sm.statsbar(s), (j / NS) & 1, timeout);
           const float* st = sm.stats(s);
-          float part = pass2_thread<ES, NCT>(sm.tbuf(s), target_slice<ES>(P, info), sm.dbuf(s),
-                                             draft_slice<ES>(P, info), sc, st[0], st[4], st[6],
-                                             ct);
+          const float ht = st[0], hd = st[4], delta = st[6];
+          const Slice s_t = target_slice<ES>(P, info);
+          const Slice s_d = draft_slice<ES>(P, info);
+          float part;
+          if (slice_aligned<ES>(s_t) && slice_aligned<ES>(s_d)) {
+            // k_d = h_d + delta as hi + lo (two-sum, exact)
+            const float kd_hi = hd + delta;
+            const float kd_lo = (hd - kd_hi) + delta;
+            const int32_t nv = s_t.nbytes >> 4;
+            if (fabsf(ht) < 64.f && fabsf(kd_hi) < 64.f)
+              part = pass2_aligned<ES, NT2, true>(sm.tbuf(s), sm.dbuf(s), nv, sc, ht, kd_hi, 0.f,
+                                                  ct);
+            else
+              part = pass2_aligned<ES, NT2, false>(sm.tbuf(s), sm.dbuf(s), nv, sc, ht, kd_hi,
+                                                   kd_lo, ct);
+          } else {
+            part = pass2_thread<ES, NT2>(sm.tbuf(s), s_t, sm.dbuf(s), s_d, sc, ht, hd, delta, ct);
+          }
           part = warp_sum_f32(part);
-          if (lane == 0) sm.cp(s)[warp] = part;
+          if (lane == 0) sm.cp(s)[warp - NW1] = part;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(sm.empty(s));
@@ -478,7 +552,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         const RowInfo pj = *sm.info(s);
         if (NEED_CONF && pj.pair) {  // label partial of unit j
           float cs = 0.f;
-          for (int w = 0; w < NCW; ++w) cs += sm.cp(s)[w];
+          for (int w = 0; w < NW2; ++w) cs += sm.cp(s)[w];
           P.cpart[static_cast<size_t>(pj.g) * kMaxSlices + pj.k] = cs / sm.stats(s)[1];
         }
         if (j + NS < n_units) produce_unit<ES>(P, sm, offs, c + (j + NS) * N, s);
@@ -494,7 +568,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
       const RowInfo info = *sm.info(s);
       RStat b_t = rstat_empty(), b_d = rstat_empty();
       int flags = 0;
-      if (lane < NCW) {
+      if (lane < NW1) {
         const float* w = sm.part(s, lane);
         b_t = RStat{w[R_HT], w[R_ST], w[R_MT], __float_as_int(w[R_IT])};
         b_d = RStat{w[R_HD], w[R_SD], w[R_MD], __float_as_int(w[R_ID])};

@@ -219,10 +219,32 @@ def test_host_errors_through_binding(cuda_lib):
         cuda_lib.verify_workload(w, max_len=0)
 
 
+@contextmanager
+def stages(n):
+    old = os.environ.get("SPEC_VERIFY_STAGES")
+    os.environ["SPEC_VERIFY_STAGES"] = str(n)
+    try:
+        yield
+    finally:
+        if old is None:
+            os.environ.pop("SPEC_VERIFY_STAGES", None)
+        else:
+            os.environ["SPEC_VERIFY_STAGES"] = old
+
+
+@pytest.mark.parametrize("L", [None, 2504])
+def test_minimum_stage_count(cuda_lib, L):
+    """Four shared-memory stages (the fewest the pipeline's barrier order
+    allows) with many units per CTA."""
+    w = W.make_workload(W.WORKLOADS[3], W.SAMPLE, seed=21, device=DEV, B=48, V=20000)
+    with stages(4), slice_len(L):
+        run_and_compare(cuda_lib, w)
+
+
 def test_deterministic_across_runs_and_slice_lengths(cuda_lib):
     w = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=13, device=DEV, B=8, V=40000)
     first = None
-    for L in (None, None, 13000, 10000, 2504, 1256):
+    for L in (None, None, 10000, 6000, 2504, 1256):
         with slice_len(L):
             out = cuda_lib.verify_workload(w, want_stats=True)
         torch.cuda.synchronize()
