@@ -357,13 +357,16 @@ int run_rows(const Args& a) {
   const bool need_z = a.mode == SV_SAMPLE || a.out_conf != nullptr || a.out_row_stats != nullptr;
   const bool need_conf = a.out_conf != nullptr;
   const bool track = a.mode == SV_GREEDY || a.out_row_stats != nullptr;
-  const int ncw = env_int("SPEC_VERIFY_WARPS", 16) <= 8 ? 8 : 16;
+  // consumer warps (16 or 24) and, with labels, how many of them run pass 1
+  // (SPEC_VERIFY_WARPS, SPEC_VERIFY_PASS1_WARPS)
+  const int ncw = env_int("SPEC_VERIFY_WARPS", 16) >= 24 ? 24 : 16;
+  P.nw1 = std::max(1, std::min(ncw - 1, env_int("SPEC_VERIFY_PASS1_WARPS", ncw / 2)));
   cudaStream_t st = static_cast<cudaStream_t>(a.stream);
   if (es == 2)
-    return ncw == 8 ? launch_rows<2, 8>(P, smem, dc, need_z, need_conf, track, st)
-                    : launch_rows<2, 16>(P, smem, dc, need_z, need_conf, track, st);
-  return ncw == 8 ? launch_rows<4, 8>(P, smem, dc, need_z, need_conf, track, st)
-                  : launch_rows<4, 16>(P, smem, dc, need_z, need_conf, track, st);
+    return ncw == 24 ? launch_rows<2, 24>(P, smem, dc, need_z, need_conf, track, st)
+                     : launch_rows<2, 16>(P, smem, dc, need_z, need_conf, track, st);
+  return ncw == 24 ? launch_rows<4, 24>(P, smem, dc, need_z, need_conf, track, st)
+                   : launch_rows<4, 16>(P, smem, dc, need_z, need_conf, track, st);
 }
 
 int run_finalize(const Args& a) {

@@ -58,6 +58,7 @@ struct Params {
   int32_t rowbuf4;   // bytes of one row buffer in shared memory (finalize kernel)
   int32_t nstages;   // shared-memory stages of the rows kernel
   int32_t offs_smem; // row_offsets copied into shared memory (B + 1 <= kMaxSmemOffsets)
+  int32_t nw1;       // rows kernel, labels on: consumer warps running pass 1
 };
 
 __device__ __forceinline__ void raise_error(const Params& P, int bits) {

@@ -63,7 +63,7 @@ constexpr int kMaxStages = 6;
 // unit and a publisher every kPublishers-th, so their previous unit implies
 // the stage's previous use is done only when stages >= both counts.
 constexpr int kMinStages = 4;
-constexpr int kMaxConsumerWarps = 16;
+constexpr int kMaxConsumerWarps = 24;
 constexpr int kPublishers = 2;
 constexpr int kGatherers = 4;
 static_assert(kMinStages >= kGatherers && kMinStages >= kPublishers, "stage reuse order");
@@ -80,7 +80,7 @@ constexpr int kOffPart = 256;                                 // [stage][warp][1
 constexpr int kOffCp = kOffPart + kMaxStages * kMaxConsumerWarps * 64;  // [stage][warp] floats
 constexpr int kOffStats = kOffCp + kMaxStages * kMaxConsumerWarps * 4;  // [stage][8] words
 constexpr int kOffInfo = kOffStats + kMaxStages * 32;                   // [stage] RowInfo
-constexpr int kRowsHdrBytes = 8192;
+constexpr int kRowsHdrBytes = 12288;
 static_assert(kOffStatsBar + 8 * kMaxStages <= kOffPart, "rows kernel barriers");
 static_assert(kOffInfo + kMaxStages * 64 <= kRowsHdrBytes, "rows kernel header");
 
@@ -157,9 +157,9 @@ __device__ __forceinline__ float sum_exp2(const float* x, float sc, float h) {
 // slice.  TRACK: exact running max / argmax.  Otherwise the reference h is
 // taken from the thread's first vector holding a finite value; an overflow or
 // a non-finite input sends the thread to the tracked variant (rare).
-template <int ES, int NCT, bool NEED_Z, bool TRACK>
+template <int ES, bool NEED_Z, bool TRACK>
 __device__ __forceinline__ RStat pass1_thread(const unsigned char* buf, const Slice& s, float sc,
-                                              int ct, bool& bad) {
+                                              int ct, int NCT, bool& bad) {
   constexpr int VEC = 16 / ES;
   const int32_t nv = s.nbytes >> 4;
   const int32_t idbase = s.v0 - s.hoff;
@@ -237,9 +237,9 @@ __device__ __forceinline__ float2 sum_exp2_x2(const float* x, float2 sc2, float2
 // lanes' first vectors), so the warp's partials are plain sums.  Returns
 // false, uniformly over the warp, on a non-finite input or an overflow (the
 // caller then runs the general path).
-template <int ES, int NT1>
+template <int ES>
 __device__ __forceinline__ bool pass1_pair_fast(const unsigned char* bt, const unsigned char* bd,
-                                                int32_t nv, float sc, int ct, RStat& at,
+                                                int32_t nv, float sc, int ct, int NT1, RStat& at,
                                                 RStat& ad) {
   constexpr int VEC = 16 / ES;
   float t[VEC], d[VEC];
@@ -285,10 +285,10 @@ __device__ __forceinline__ bool pass1_pair_fast(const unsigned char* bt, const u
 // vectors, a = t sc - h_t, b = d sc - k_d with k_d = h_d + delta.  kd_hi +
 // kd_lo represents k_d exactly; when kd_lo is 0 (FOLD) the subtraction
 // disappears (the caller folds only when that costs at most ~2e-6 in c*).
-template <int ES, int NT2, bool FOLD>
+template <int ES, bool FOLD>
 __device__ __forceinline__ float pass2_aligned(const unsigned char* bt, const unsigned char* bd,
                                                int32_t nv, float sc, float ht, float kd_hi,
-                                               float kd_lo, int ct) {
+                                               float kd_lo, int ct, int NT2) {
   constexpr int VEC = 16 / ES;
   const float2 sc2 = make_float2(sc, sc), nht = make_float2(-ht, -ht),
                nkd = make_float2(-kd_hi, -kd_hi), nlo = make_float2(-kd_lo, -kd_lo);
@@ -315,10 +315,10 @@ __device__ __forceinline__ float pass2_aligned(const unsigned char* bt, const un
 
 // Pass 2, general path (slices with masked ends or different 16-byte phases):
 // sum of exp2(min(a, b - delta)) over the thread's elements.
-template <int ES, int NT2>
+template <int ES>
 __device__ __forceinline__ float pass2_thread(const unsigned char* bt, const Slice& st_,
                                               const unsigned char* bd, const Slice& sd_, float sc,
-                                              float ht, float hd, float delta, int ct) {
+                                              float ht, float hd, float delta, int ct, int NT2) {
   constexpr int VEC = 16 / ES;
   float acc = 0.f;
   if (st_.hoff == sd_.hoff) {  // same vector grid: vectorised, masked ends
@@ -436,10 +436,11 @@ constexpr int rows_threads(int ncw) { return (ncw + 1 + kPublishers + kGatherers
 
 template <int ES, int NCW, bool NEED_Z, bool NEED_CONF, bool TRACK>
 __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params P) {
-  static_assert(NCW <= kMaxConsumerWarps && NCW % 2 == 0, "consumer warps");
-  constexpr int NW1 = NEED_CONF ? NCW / 2 : NCW;  // pass-1 warps
-  constexpr int NW2 = NCW - NW1;                  // pass-2 warps
-  constexpr int NT1 = NW1 * 32, NT2 = NW2 > 0 ? NW2 * 32 : 32;
+  static_assert(NCW <= kMaxConsumerWarps, "consumer warps");
+  // pass-1 warps [0, NW1), pass-2 warps [NW1, NCW) (labels on)
+  const int NW1 = NEED_CONF ? P.nw1 : NCW;
+  const int NW2 = NCW - NW1;
+  const int NT1 = NW1 * 32, NT2 = NW2 > 0 ? NW2 * 32 : 32;
   constexpr int W_PROD = NCW, W_PUB = NCW + 1, W_GATH = NCW + 1 + kPublishers;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const RowsSmem sm{smem_raw, P.rowbuf};
@@ -490,11 +491,11 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         RStat a_t, a_d;
         const bool fast = !TRACK && NEED_Z && info.pair && slice_aligned<ES>(s_t) &&
                           slice_aligned<ES>(s_d) &&
-                          pass1_pair_fast<ES, NT1>(sm.tbuf(s), sm.dbuf(s), s_t.nbytes >> 4, sc, ct,
-                                                   a_t, a_d);
+                          pass1_pair_fast<ES>(sm.tbuf(s), sm.dbuf(s), s_t.nbytes >> 4, sc, ct, NT1,
+                                              a_t, a_d);
         if (!fast) {  // general path: per-thread partials, then a warp merge
-          a_t = pass1_thread<ES, NT1, NEED_Z, TRACK>(sm.tbuf(s), s_t, sc, ct, bad);
-          a_d = info.pair ? pass1_thread<ES, NT1, NEED_Z, TRACK>(sm.dbuf(s), s_d, sc, ct, bad)
+          a_t = pass1_thread<ES, NEED_Z, TRACK>(sm.tbuf(s), s_t, sc, ct, NT1, bad);
+          a_d = info.pair ? pass1_thread<ES, NEED_Z, TRACK>(sm.dbuf(s), s_d, sc, ct, NT1, bad)
                           : rstat_empty();
           a_t = rstat_warp_reduce(a_t);
           a_d = rstat_warp_reduce(a_d);
@@ -528,13 +529,13 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
             const float kd_lo = (hd - kd_hi) + delta;
             const int32_t nv = s_t.nbytes >> 4;
             if (fabsf(ht) < 64.f && fabsf(kd_hi) < 64.f)
-              part = pass2_aligned<ES, NT2, true>(sm.tbuf(s), sm.dbuf(s), nv, sc, ht, kd_hi, 0.f,
-                                                  ct);
+              part = pass2_aligned<ES, true>(sm.tbuf(s), sm.dbuf(s), nv, sc, ht, kd_hi, 0.f, ct,
+                                             NT2);
             else
-              part = pass2_aligned<ES, NT2, false>(sm.tbuf(s), sm.dbuf(s), nv, sc, ht, kd_hi,
-                                                   kd_lo, ct);
+              part = pass2_aligned<ES, false>(sm.tbuf(s), sm.dbuf(s), nv, sc, ht, kd_hi, kd_lo,
+                                              ct, NT2);
           } else {
-            part = pass2_thread<ES, NT2>(sm.tbuf(s), s_t, sm.dbuf(s), s_d, sc, ht, hd, delta, ct);
+            part = pass2_thread<ES>(sm.tbuf(s), s_t, sm.dbuf(s), s_d, sc, ht, hd, delta, ct, NT2);
           }
           part = warp_sum_f32(part);
           if (lane == 0) sm.cp(s)[warp - NW1] = part;

@@ -232,6 +232,32 @@ def stages(n):
             os.environ["SPEC_VERIFY_STAGES"] = old
 
 
+@contextmanager
+def env(**kw):
+    """Set SPEC_VERIFY_* knobs of the rows kernel for the duration."""
+    old = {k: os.environ.get(k) for k in kw}
+    os.environ.update({k: str(v) for k, v in kw.items()})
+    try:
+        yield
+    finally:
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+
+
+@pytest.mark.parametrize("warps,pass1", [(16, 4), (16, 12), (24, 12), (24, 16), (24, 20)])
+@pytest.mark.parametrize("L", [None, 2504])
+def test_consumer_warp_splits(cuda_lib, warps, pass1, L):
+    """Any split of the consumer warps between pass 1 and pass 2 gives the
+    oracle's results (labels on, so both groups run)."""
+    w = W.make_workload(W.WORKLOADS[3], W.SAMPLE, seed=23, device=DEV, B=24, V=30011)
+    with env(SPEC_VERIFY_WARPS=warps, SPEC_VERIFY_PASS1_WARPS=pass1), slice_len(L):
+        run_and_compare(cuda_lib, w)
+        run_and_compare(cuda_lib, w, mode=W.GREEDY, want_conf=False, want_stats=True)
+
+
 @pytest.mark.parametrize("L", [None, 2504])
 def test_minimum_stage_count(cuda_lib, L):
     """Four shared-memory stages (the fewest the pipeline's barrier order
