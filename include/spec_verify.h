@@ -75,6 +75,7 @@ extern "C" {
 #define SV_ERR_CUDA (-3)        /* a CUDA runtime call or a launch failed */
 #define SV_ERR_UNSUPPORTED (-4) /* filter combination or cluster shape not available */
 #define SV_ERR_WORKSPACE (-5)   /* workspace missing, misaligned or too small */
+#define SV_ERR_TOO_LARGE (-6)   /* spec_verify_static: more than SV_STATIC_MAX_ROWS rows */
 
 /* device error bits OR-ed into *dev_error */
 #define SV_DEVERR_NAN 1     /* a row holds NaN or +inf, or is entirely -inf */
@@ -85,6 +86,7 @@ extern "C" {
 /* limits */
 #define SV_MAX_LEN 256       /* largest accepted max_len */
 #define SV_MAX_FILTER_K 64   /* largest top_k served together with top_p < 1 */
+#define SV_STATIC_MAX_ROWS 4096 /* largest n_target_rows of spec_verify_static */
 
 /*
  * Bytes of workspace a call with these sizes needs (a multiple of 256).
@@ -172,6 +174,37 @@ int spec_verify_finalize(const void* target_logits, const void* draft_logits,
                          int32_t mode, int32_t* out_tokens, int32_t* out_accept_len,
                          float* out_conf, float* out_row_stats, int32_t* dev_error,
                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * spec_verify without a workspace argument, for callers that cannot allocate
+ * device memory when they verify (a plain-C host loop without a caching
+ * allocator, where cudaMalloc / cudaFree would synchronise the device every
+ * step; a process whose memory is committed up front to other pools).  The
+ * source pages have no counterpart of this call: it is an interface
+ * convenience, and computes exactly what spec_verify computes.
+ *
+ * Scratch is a file-scope device array of this library sized for
+ * SV_STATIC_MAX_ROWS target rows (about 17.4 MB of device memory, reserved
+ * when the library's module is loaded on a device).  Nothing is allocated by
+ * the call.  n_target_rows > SV_STATIC_MAX_ROWS returns SV_ERR_TOO_LARGE
+ * before anything is enqueued.
+ *
+ * The first call on a device (with that device current) looks up the
+ * array's address and enqueues a clear of it on `stream`; make that first
+ * call before capturing any stream into a CUDA graph.  The array is shared by
+ * every call on the device: calls whose GPU work can overlap (different
+ * streams without ordering, concurrent host threads) race on it and must be
+ * serialised by the caller.  All other arguments, outputs and errors are as
+ * for spec_verify.
+ */
+int spec_verify_static(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const float* uniforms,
+                       const int32_t* verify_lens, const int32_t* row_offsets,
+                       int32_t B, int32_t V, int32_t n_target_rows, int32_t max_len,
+                       int32_t dtype, float temperature, int32_t top_k, float top_p,
+                       int32_t mode, int32_t* out_tokens, int32_t* out_accept_len,
+                       float* out_conf, float* out_row_stats, int32_t* dev_error,
+                       void* stream);
 
 /* Static text for a status code (host). */
 const char* spec_verify_status_string(int status);

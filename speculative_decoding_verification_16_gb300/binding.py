@@ -26,6 +26,8 @@ _lib = ctypes.CDLL(LIB_PATH)
 SV_BF16, SV_FP32 = 0, 1
 SV_GREEDY, SV_SAMPLE = 0, 1
 SV_OK = 0
+SV_ERR_TOO_LARGE = -6
+SV_STATIC_MAX_ROWS = 4096
 SV_DEVERR_NAN, SV_DEVERR_TOKEN, SV_DEVERR_LEN, SV_DEVERR_TIMEOUT = 1, 2, 4, 8
 
 _vp, _i32, _f32, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float, ctypes.c_size_t
@@ -38,6 +40,8 @@ for _name in ("spec_verify", "spec_verify_rows", "spec_verify_finalize"):
     _fn = getattr(_lib, _name)
     _fn.argtypes = _ARGTYPES
     _fn.restype = ctypes.c_int
+_lib.spec_verify_static.argtypes = _ARGTYPES[:20] + [_vp]   # no workspace arguments
+_lib.spec_verify_static.restype = ctypes.c_int
 _lib.spec_verify_workspace_size.argtypes = [_i32, _i32]
 _lib.spec_verify_workspace_size.restype = ctypes.c_size_t
 _lib.spec_verify_status_string.argtypes = [ctypes.c_int]
@@ -163,6 +167,33 @@ def spec_verify(target_logits, draft_logits, draft_tokens, uniforms, verify_lens
     prepare("spec_verify", target_logits, draft_logits, draft_tokens, uniforms, verify_lens,
             row_offsets, max_len=max_len, temperature=temperature, top_k=top_k, top_p=top_p,
             mode=mode, out=out, workspace=workspace, stream=stream)()
+    return out
+
+
+def spec_verify_static(target_logits, draft_logits, draft_tokens, uniforms, verify_lens,
+                       row_offsets, *, max_len=16, temperature=1.0, top_k=0, top_p=1.0,
+                       mode=SV_SAMPLE, out: Outputs, stream=None) -> Outputs:
+    """The C entry point that allocates nothing (scratch in the library's
+    static device array).  ``out`` must be given: this path allocates no
+    device memory, not even through torch."""
+    for t in (target_logits, draft_logits, draft_tokens, uniforms, verify_lens, row_offsets):
+        if not t.is_contiguous():
+            raise ValueError("inputs must be contiguous")
+    B = verify_lens.numel()
+    n_target_rows, V = target_logits.shape
+    if stream is None:
+        stream = torch.cuda.current_stream(target_logits.device)
+    rc = _lib.spec_verify_static(
+        _ptr(target_logits), _ptr(draft_logits) if draft_logits.numel() else None,
+        _ptr(draft_tokens) if draft_tokens.numel() else None, _ptr(uniforms),
+        _ptr(verify_lens), _ptr(row_offsets),
+        _i32(B), _i32(V), _i32(n_target_rows), _i32(max_len),
+        _i32(_dtype_code(target_logits)), _f32(temperature), _i32(top_k), _f32(top_p),
+        _i32(mode),
+        _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.conf), _ptr(out.row_stats),
+        _ptr(out.dev_error), ctypes.c_void_p(stream.cuda_stream))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc)
     return out
 
 

@@ -12,6 +12,7 @@
 #include <algorithm>
 #include <atomic>
 #include <mutex>
+#include <unordered_map>
 
 #include "spec_verify.h"
 #include "sv_common.cuh"
@@ -397,6 +398,48 @@ int run_finalize(const Args& a) {
                         st);
 }
 
+// ---------------------------------------------------------------- static scratch
+// Scratch of spec_verify_static: the same three workspace regions as a caller
+// workspace (row records, label partials, published pass-1 partials), sized
+// for SV_STATIC_MAX_ROWS target rows (about 17.4 MB), in a file-scope device
+// array so that the call needs no allocation.  Some callers cannot allocate
+// device memory at the point where they verify: a host loop in plain C with
+// no caching allocator, where cudaMalloc / cudaFree would synchronise the
+// whole device on every step, or a process whose memory is fully committed
+// to a weight and KV-cache pool up front.  The array belongs to this module:
+// two spec_verify_static calls that overlap on the GPU (different streams,
+// or different host threads without ordering) share it and race.
+constexpr size_t round256(size_t b) { return (b + 255) / 256 * 256; }
+constexpr size_t kStaticBytes =
+    round256(round256(static_cast<size_t>(SV_STATIC_MAX_ROWS) * sizeof(RowRec)) +
+             round256(static_cast<size_t>(SV_STATIC_MAX_ROWS) * kMaxSlices * sizeof(float)) +
+             static_cast<size_t>(SV_STATIC_MAX_ROWS) * kMaxSlices * kPartWords * 8) +
+    256;
+
+__device__ __align__(256) unsigned char g_static_ws[kStaticBytes];
+
+std::mutex g_static_mu;
+std::unordered_map<int, void*> g_static_ptr;  // device ordinal -> address of g_static_ws
+
+// Address of this device's static scratch.  The first call on a device looks
+// the address up and clears the published-partials region (its words must
+// not carry a live call tag; zero never is one) on `stream`, ahead of the
+// kernels of the same call.
+int static_workspace(void** out, cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  auto it = g_static_ptr.find(dev);
+  if (it == g_static_ptr.end()) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || p == nullptr) return SV_ERR_CUDA;
+    if (cudaMemsetAsync(p, 0, kStaticBytes, stream) != cudaSuccess) return SV_ERR_CUDA;
+    it = g_static_ptr.emplace(dev, p).first;
+  }
+  *out = it->second;
+  return SV_OK;
+}
+
 }  // namespace
 }  // namespace sv
 
@@ -443,6 +486,28 @@ int spec_verify(SV_ARGS_DECL) {
   return rc;
 }
 
+int spec_verify_static(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, const float* uniforms,
+                       const int32_t* verify_lens, const int32_t* row_offsets, int32_t B,
+                       int32_t V, int32_t n_target_rows, int32_t max_len, int32_t dtype,
+                       float temperature, int32_t top_k, float top_p, int32_t mode,
+                       int32_t* out_tokens, int32_t* out_accept_len, float* out_conf,
+                       float* out_row_stats, int32_t* dev_error, void* stream) {
+  if (n_target_rows > SV_STATIC_MAX_ROWS ||
+      spec_verify_workspace_size(B, n_target_rows) > sv::kStaticBytes)
+    return SV_ERR_TOO_LARGE;
+  void* ws = nullptr;
+  int rc = sv::static_workspace(&ws, static_cast<cudaStream_t>(stream));
+  if (rc != SV_OK) return rc;
+  const size_t workspace_bytes = sv::kStaticBytes;
+  void* workspace = ws;
+  SV_ARGS_PACK;
+  rc = sv::check_args(a);
+  if (rc == SV_OK) rc = sv::run_rows(a);
+  if (rc == SV_OK) rc = sv::run_finalize(a);
+  return rc;
+}
+
 const char* spec_verify_status_string(int status) {
   switch (status) {
     case SV_OK: return "ok";
@@ -451,6 +516,9 @@ const char* spec_verify_status_string(int status) {
     case SV_ERR_CUDA: return "CUDA runtime or launch failure";
     case SV_ERR_UNSUPPORTED: return "filter combination or cluster shape not supported";
     case SV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SV_ERR_TOO_LARGE:
+      return "problem larger than the static scratch of spec_verify_static "
+             "(more than SV_STATIC_MAX_ROWS target rows)";
     default: return "unknown status";
   }
 }

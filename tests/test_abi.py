@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings(lib):
     lib.spec_verify_status_string.restype = ctypes.c_char_p
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert lib.spec_verify_status_string(code)
     assert lib.spec_verify_status_string(123) == b"unknown status"
 
@@ -108,3 +108,17 @@ def test_greedy_without_labels_accepts_any_temperature(lib):
     # checks pass, so the call reaches the device stage; stop it there by an
     # undersized workspace to keep this a host-only test.
     assert _call(lib, mode=0, T=0.0, out_conf=None, ws_bytes=64) == -5
+
+
+def test_static_entry_rejects_oversized_problem_before_any_device_call(lib):
+    """The no-allocation entry point refuses more target rows than its static
+    scratch holds, before it looks up a device."""
+    fake = 1 << 20
+    f = lib.spec_verify_static
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+    f.argtypes = [vp] * 6 + [i32] * 4 + [i32, f32, i32, f32, i32] + [vp] * 5 + [vp]
+    f.restype = ctypes.c_int
+    B, max_len = 512, 16
+    for nt, code in ((4097, -6), (8192, -6)):
+        assert f(fake, fake, fake, fake, fake, fake, B, 151936, nt, max_len, 0, 1.0, 0, 1.0, 1,
+                 fake, fake, fake, None, None, None) == code
