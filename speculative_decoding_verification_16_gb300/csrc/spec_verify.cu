@@ -352,6 +352,7 @@ int run_rows(const Args& a) {
   P.nstages = geo.stages;
   P.tag = next_tag();
   P.offs_smem = geo.offs_smem;
+  P.poll_ns = std::max(0, std::min(10000, env_int("SPEC_VERIFY_POLL_NS", 128)));
   const int smem = geo.smem;
   // z is needed for sampling, labels and statistics; the exact max / argmax
   // only for greedy decisions and statistics

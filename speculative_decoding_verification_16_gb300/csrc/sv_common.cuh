@@ -59,6 +59,7 @@ struct Params {
   int32_t nstages;   // shared-memory stages of the rows kernel
   int32_t offs_smem; // row_offsets copied into shared memory (B + 1 <= kMaxSmemOffsets)
   int32_t nw1;       // rows kernel, labels on: consumer warps running pass 1
+  int32_t poll_ns;   // rows kernel: gatherer sleep between polls
 };
 
 __device__ __forceinline__ void raise_error(const Params& P, int bits) {

@@ -120,17 +120,32 @@ __device__ __forceinline__ float warp_sum_f32(float v) {
   return v;
 }
 
-// Merge the 32 lanes' partials: max reference, one rescale each, plain sum;
-// argmax = lowest id among lanes holding the largest maximum.  Every lane
+// Merge two statistics (a target and a draft row) over the 32 lanes'
+// partials: max reference, one rescale each, plain sum (the two dependency
+// chains interleaved); with TRACK also the max and the lowest id holding it
+// (without TRACK those fields are unused and left as they are).  Every lane
 // gets the same bits.
-__device__ __forceinline__ RStat rstat_warp_reduce(const RStat& a) {
-  RStat r;
-  r.h = warp_max_f32(a.h);
-  const float part = (a.h == -INFINITY) ? 0.f : a.s * ex2(a.h - r.h);
-  r.s = r.h == -INFINITY ? 0.f : warp_sum_f32(part);
-  r.m = warp_max_f32(a.m);
-  r.i = __reduce_min_sync(0xffffffffu, a.m == r.m ? a.i : 0x7fffffff);
-  return r;
+template <bool TRACK>
+__device__ __forceinline__ void rstat_warp_reduce2(RStat& a, RStat& b) {
+  const float ha = warp_max_f32(a.h), hb = warp_max_f32(b.h);
+  float sa = a.h == -INFINITY ? 0.f : a.s * ex2(a.h - ha);
+  float sb = b.h == -INFINITY ? 0.f : b.s * ex2(b.h - hb);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sa += __shfl_xor_sync(0xffffffffu, sa, off);
+    sb += __shfl_xor_sync(0xffffffffu, sb, off);
+  }
+  a.s = ha == -INFINITY ? 0.f : sa;
+  b.s = hb == -INFINITY ? 0.f : sb;
+  a.h = ha;
+  b.h = hb;
+  if (TRACK) {
+    const float ma = warp_max_f32(a.m), mb = warp_max_f32(b.m);
+    a.i = __reduce_min_sync(0xffffffffu, a.m == ma ? a.i : 0x7fffffff);
+    b.i = __reduce_min_sync(0xffffffffu, b.m == mb ? b.i : 0x7fffffff);
+    a.m = ma;
+    b.m = mb;
+  }
 }
 
 template <int VEC>
@@ -399,25 +414,72 @@ struct RowsSmem {
   __device__ __forceinline__ unsigned char* dbuf(int s) const { return tbuf(s) + rowbuf; }
 };
 
-// Producer step (one lane): load unit u into stage s.  The stage's `full`
-// barrier completes when the bulk copies' bytes have landed and the row
-// metadata copied by cp.async has arrived.
+// What the producer needs to issue a unit, worked out ahead of time: the
+// producer warp plans 32 units at once (one per lane) while it waits for
+// stages, so that issuing a unit into a freed stage is a handful of
+// instructions (the single-lane search and address arithmetic would
+// otherwise delay every refill by a few thousand cycles).
+struct UnitPlan {
+  int32_t g, k, r, off, off1, pair, gd;
+  int32_t tn, dn;                // bytes of the target / draft copies
+  const unsigned char* ts;       // their 16-byte-aligned sources
+  const unsigned char* ds;
+};
+
 template <int ES>
-__device__ __forceinline__ void produce_unit(const Params& P, const RowsSmem& sm,
-                                             const int32_t* offs, int32_t u, int s) {
+__device__ __forceinline__ UnitPlan plan_unit(const Params& P, const int32_t* offs, int32_t u) {
+  RowInfo info;
+  locate_row(P, offs, u / P.nslices, &info);
+  info.k = u % P.nslices;
+  const Slice st = target_slice<ES>(P, info);
+  const Slice sd = draft_slice<ES>(P, info);
+  return UnitPlan{info.g, info.k, info.r, info.off, info.off1, info.pair, info.gd,
+                  st.nbytes,  sd.nbytes, st.gsrc, sd.gsrc};
+}
+
+// The plan held by lane `src` of the producer warp, on every lane.
+__device__ __forceinline__ UnitPlan shfl_plan(const UnitPlan& p, int src) {
+  constexpr unsigned F = 0xffffffffu;
+  UnitPlan q;
+  q.g = __shfl_sync(F, p.g, src);
+  q.k = __shfl_sync(F, p.k, src);
+  q.r = __shfl_sync(F, p.r, src);
+  q.off = __shfl_sync(F, p.off, src);
+  q.off1 = __shfl_sync(F, p.off1, src);
+  q.pair = __shfl_sync(F, p.pair, src);
+  q.gd = __shfl_sync(F, p.gd, src);
+  q.tn = __shfl_sync(F, p.tn, src);
+  q.dn = __shfl_sync(F, p.dn, src);
+  q.ts = reinterpret_cast<const unsigned char*>(
+      __shfl_sync(F, reinterpret_cast<unsigned long long>(p.ts), src));
+  q.ds = reinterpret_cast<const unsigned char*>(
+      __shfl_sync(F, reinterpret_cast<unsigned long long>(p.ds), src));
+  return q;
+}
+
+// Producer step (one lane): load the planned unit into stage s.  The stage's
+// `full` barrier completes when the bulk copies' bytes have landed and the
+// row metadata copied by cp.async has arrived.
+template <int ES>
+__device__ __forceinline__ void issue_unit(const Params& P, const RowsSmem& sm, const UnitPlan& p,
+                                           int s) {
   RowInfo* info = sm.info(s);
-  locate_row(P, offs, u / P.nslices, info);
-  info->k = u % P.nslices;
-  const RowInfo cur = *info;
-  const Slice st = target_slice<ES>(P, cur);
-  const Slice sd = draft_slice<ES>(P, cur);
+  info->g = p.g;
+  info->k = p.k;
+  info->r = p.r;
+  info->off = p.off;
+  info->off1 = p.off1;
+  info->pair = p.pair;
+  info->gd = p.gd;
+  info->x = -1;
+  info->ell = 0;
   const uint32_t bar = sm.full(s);
-  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(st.nbytes + sd.nbytes));
-  if (st.nbytes) bulk_g2s(smem_addr(sm.tbuf(s)), st.gsrc, st.nbytes, bar);
-  if (sd.nbytes) bulk_g2s(smem_addr(sm.dbuf(s)), sd.gsrc, sd.nbytes, bar);
-  cp_async4(smem_addr(&info->u), P.uniforms + cur.g);
-  cp_async4(smem_addr(&info->ell), P.lens + cur.r);
-  if (cur.pair) cp_async4(smem_addr(&info->x), P.draft_tokens + cur.gd);
+  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tn + p.dn));
+  if (p.tn) bulk_g2s(smem_addr(sm.tbuf(s)), p.ts, p.tn, bar);
+  if (p.dn) bulk_g2s(smem_addr(sm.dbuf(s)), p.ds, p.dn, bar);
+  cp_async4(smem_addr(&info->u), P.uniforms + p.g);
+  cp_async4(smem_addr(&info->ell), P.lens + p.r);
+  if (p.pair) cp_async4(smem_addr(&info->x), P.draft_tokens + p.gd);
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
@@ -462,15 +524,24 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
     offs = offs_sm;
   }
   __syncthreads();
-  if (warp == W_PROD && lane == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(sm.full(s), 2);                 // bulk-copy arm + cp.async completion
-      mbar_init(sm.empty(s), (NEED_CONF ? NW2 : NW1) + 2);  // + publisher + gatherer
-      mbar_init(sm.partbar(s), NW1);
-      mbar_init(sm.statsbar(s), 1);
+  // producer warp: plans of units [plan_base, plan_base + 32), one per lane
+  UnitPlan plan{};
+  int32_t plan_base = 0;
+  if (warp == W_PROD) {
+    if (lane == 0) {
+      for (int s = 0; s < NS; ++s) {
+        mbar_init(sm.full(s), 2);                 // bulk-copy arm + cp.async completion
+        mbar_init(sm.empty(s), (NEED_CONF ? NW2 : NW1) + 2);  // + publisher + gatherer
+        mbar_init(sm.partbar(s), NW1);
+        mbar_init(sm.statsbar(s), 1);
+      }
+      fence_mbar_init();
     }
-    fence_mbar_init();
-    for (int i = 0; i < NS && i < n_units; ++i) produce_unit<ES>(P, sm, offs, c + i * N, i);
+    if (lane < n_units) plan = plan_unit<ES>(P, offs, c + lane * N);
+    for (int i = 0; i < NS && i < n_units; ++i) {
+      const UnitPlan q = shfl_plan(plan, i);
+      if (lane == 0) issue_unit<ES>(P, sm, q, i);
+    }
   }
   __syncthreads();
 
@@ -497,8 +568,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
           a_t = pass1_thread<ES, NEED_Z, TRACK>(sm.tbuf(s), s_t, sc, ct, NT1, bad);
           a_d = info.pair ? pass1_thread<ES, NEED_Z, TRACK>(sm.dbuf(s), s_d, sc, ct, NT1, bad)
                           : rstat_empty();
-          a_t = rstat_warp_reduce(a_t);
-          a_d = rstat_warp_reduce(a_d);
+          rstat_warp_reduce2<true>(a_t, a_d);
         }
         const unsigned badw = __ballot_sync(0xffffffffu, bad);
         if (lane == 0) {
@@ -546,17 +616,28 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
     }
   } else if (warp == W_PROD) {
     // =============================== producer warp
+    // After unit j releases stage s: write unit j's label partial and issue
+    // unit j + NS into the stage.  Plans for the next 32 units are made
+    // (all lanes, one unit each) before waiting, off the refill's path.
     for (int32_t j = 0; j < n_units; ++j) {
       const int s = j % NS;
+      const int32_t nxt = j + NS;
+      if (nxt < n_units && nxt >= plan_base + 32) {
+        plan_base += 32;
+        if (plan_base + lane < n_units) plan = plan_unit<ES>(P, offs, c + (plan_base + lane) * N);
+      }
       mbar_wait(sm.empty(s), (j / NS) & 1, timeout);
+      const UnitPlan q = shfl_plan(plan, (nxt - plan_base) & 31);
       if (lane == 0) {
-        const RowInfo pj = *sm.info(s);
-        if (NEED_CONF && pj.pair) {  // label partial of unit j
-          float cs = 0.f;
+        const RowInfo* pj = sm.info(s);
+        const int32_t pg = pj->g, pk = pj->k, ppair = pj->pair;
+        float cs = 0.f, z = 1.f;
+        if (NEED_CONF && ppair) {  // label partial of unit j (read before the refill)
           for (int w = 0; w < NW2; ++w) cs += sm.cp(s)[w];
-          P.cpart[static_cast<size_t>(pj.g) * kMaxSlices + pj.k] = cs / sm.stats(s)[1];
+          z = sm.stats(s)[1];
         }
-        if (j + NS < n_units) produce_unit<ES>(P, sm, offs, c + (j + NS) * N, s);
+        if (nxt < n_units) issue_unit<ES>(P, sm, q, s);
+        if (NEED_CONF && ppair) P.cpart[static_cast<size_t>(pg) * kMaxSlices + pk] = cs / z;
       }
       __syncwarp();
     }
@@ -575,8 +656,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         b_d = RStat{w[R_HD], w[R_SD], w[R_MD], __float_as_int(w[R_ID])};
         flags = __float_as_int(w[R_BAD]);
       }
-      b_t = rstat_warp_reduce(b_t);
-      b_d = rstat_warp_reduce(b_d);
+      rstat_warp_reduce2<TRACK>(b_t, b_d);
       flags = __reduce_or_sync(0xffffffffu, flags);
       const Slice s_t = target_slice<ES>(P, info);
       const bool hasx = info.pair && info.x >= s_t.v0 && info.x < s_t.v0 + s_t.len;
@@ -585,23 +665,20 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         xt = slice_elem<ES>(sm.tbuf(s), s_t, info.x - s_t.v0);
         xd = slice_elem<ES>(sm.dbuf(s), draft_slice<ES>(P, info), info.x - s_t.v0);
       }
-      // lane w < R_NWORDS publishes word w of the partial, tagged
-      uint32_t word = 0;
-      switch (lane) {
-        case R_HT: word = __float_as_uint(b_t.h); break;
-        case R_ST: word = __float_as_uint(b_t.s); break;
-        case R_MT: word = __float_as_uint(b_t.m); break;
-        case R_IT: word = static_cast<uint32_t>(b_t.i); break;
-        case R_HD: word = __float_as_uint(b_d.h); break;
-        case R_SD: word = __float_as_uint(b_d.s); break;
-        case R_MD: word = __float_as_uint(b_d.m); break;
-        case R_ID: word = static_cast<uint32_t>(b_d.i); break;
-        case R_BAD: word = static_cast<uint32_t>(flags); break;
-        case R_XT: word = __float_as_uint(xt); break;
-        case R_XD: word = __float_as_uint(xd); break;
-        case R_HASX: word = hasx ? 1u : 0u; break;
-        default: break;
-      }
+      // lane w < R_NWORDS publishes word w of the partial, tagged (selects,
+      // no divergent branches)
+      uint32_t word = hasx ? 1u : 0u;
+      word = lane == R_XD ? __float_as_uint(xd) : word;
+      word = lane == R_XT ? __float_as_uint(xt) : word;
+      word = lane == R_BAD ? static_cast<uint32_t>(flags) : word;
+      word = lane == R_ID ? static_cast<uint32_t>(b_d.i) : word;
+      word = lane == R_MD ? __float_as_uint(b_d.m) : word;
+      word = lane == R_SD ? __float_as_uint(b_d.s) : word;
+      word = lane == R_HD ? __float_as_uint(b_d.h) : word;
+      word = lane == R_IT ? static_cast<uint32_t>(b_t.i) : word;
+      word = lane == R_MT ? __float_as_uint(b_t.m) : word;
+      word = lane == R_ST ? __float_as_uint(b_t.s) : word;
+      word = lane == R_HT ? __float_as_uint(b_t.h) : word;
       if (lane < R_NWORDS) {
         uint64_t* dst = parts + (static_cast<size_t>(info.g) * kMaxSlices + info.k) * kPartWords;
         st_relaxed_u64(dst + lane, tagw | word);
@@ -647,7 +724,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
             timeout = true;
             break;
           }
-          __nanosleep(256);
+          if (P.poll_ns > 0) __nanosleep(P.poll_ns);
         }
       }
       RStat gt = rstat_empty(), gdr = rstat_empty();
@@ -664,8 +741,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         xd = __uint_as_float(wv[R_XD]);
         hasx = wv[R_HASX] != 0;
       }
-      gt = rstat_warp_reduce(gt);
-      gdr = rstat_warp_reduce(gdr);
+      rstat_warp_reduce2<TRACK>(gt, gdr);
       flags = __reduce_or_sync(0xffffffffu, flags) | (timeout ? SV_DEVERR_TIMEOUT : 0);
       const unsigned xl = __ballot_sync(0xffffffffu, hasx);
       if (xl) {
