@@ -66,7 +66,7 @@ bool is_filtered(int V, int top_k, float top_p) {
 }
 
 // Geometry of the rows kernel: a row is cut into S <= kMaxSlices slices of
-// L elements (L a multiple of the 16-byte vector; about 13000 bf16 / 6500
+// L elements (L a multiple of the 16-byte vector; about 11000 bf16 / 5500
 // fp32 elements by default, SPEC_VERIFY_SLICE overrides) and as many stages
 // (kMinStages .. kMaxStages, SPEC_VERIFY_STAGES caps) as the shared memory
 // allows next to the row_offsets copy (B + 1 entries when they fit).
@@ -76,7 +76,7 @@ struct RowsGeom {
 
 int rows_geometry(int V, int B, int es, const DeviceCache& dc, RowsGeom* g) {
   const int vec = 16 / es;
-  const int target = env_int("SPEC_VERIFY_SLICE", 26000 / es);
+  const int target = env_int("SPEC_VERIFY_SLICE", 22000 / es);
   int S = std::max(1, (V + target - 1) / target);
   S = std::min(S, kMaxSlices);
   const int L = round_up((V + S - 1) / S, vec);

@@ -92,9 +92,34 @@ struct RowInfo {
   int32_t x;    // drafted token (cp.async)
   int32_t ell;  // l_r (cp.async)
   float u;      // uniform of the row (cp.async)
-  int32_t pad[6];
+  int32_t tn, dn;        // bytes of the target / draft slice buffers (dn = 0: no draft row)
+  int32_t thoff, dhoff;  // head offsets (elements) of the slices in them
+  int32_t len, v0;       // slice length, vocabulary id of its first element
 };
 static_assert(sizeof(RowInfo) == 64, "RowInfo layout");
+
+// The unit's slices as shared-memory buffer views (the global sources are
+// not needed once the stage is filled).
+__device__ __forceinline__ Slice slice_t(const RowInfo& i) {
+  return Slice{nullptr, i.tn, i.thoff, i.len, i.v0};
+}
+__device__ __forceinline__ Slice slice_d(const RowInfo& i) {
+  return Slice{nullptr, i.dn, i.dhoff, i.pair ? i.len : 0, i.v0};
+}
+
+// Position in a ring of n slots: the slot and the phase parity of its
+// current use, advanced without a division (the ring size is a runtime
+// value, and a division per step would sit on every role's critical path).
+struct RingPos {
+  int idx;
+  uint32_t par;
+  __device__ __forceinline__ void next(int n) {
+    if (++idx == n) {
+      idx = 0;
+      par ^= 1u;
+    }
+  }
+};
 
 // Partial statistics of a row: sum_v 2^(x_v * sc) = s * 2^h; m = max raw
 // logit and i = lowest id holding it (tracked variant only; m = -inf, i =
@@ -421,8 +446,8 @@ struct RowsSmem {
 // otherwise delay every refill by a few thousand cycles).
 struct UnitPlan {
   int32_t g, k, r, off, off1, pair, gd;
-  int32_t tn, dn;                // bytes of the target / draft copies
-  const unsigned char* ts;       // their 16-byte-aligned sources
+  int32_t tn, dn, thoff, dhoff, len, v0;  // slice buffers (RowInfo fields)
+  const unsigned char* ts;                // 16-byte-aligned sources of the copies
   const unsigned char* ds;
 };
 
@@ -433,8 +458,8 @@ __device__ __forceinline__ UnitPlan plan_unit(const Params& P, const int32_t* of
   info.k = u % P.nslices;
   const Slice st = target_slice<ES>(P, info);
   const Slice sd = draft_slice<ES>(P, info);
-  return UnitPlan{info.g, info.k, info.r, info.off, info.off1, info.pair, info.gd,
-                  st.nbytes,  sd.nbytes, st.gsrc, sd.gsrc};
+  return UnitPlan{info.g,  info.k,   info.r,  info.off, info.off1, info.pair, info.gd,
+                  st.nbytes, sd.nbytes, st.hoff, sd.hoff, st.len,   st.v0,     st.gsrc, sd.gsrc};
 }
 
 // The plan held by lane `src` of the producer warp, on every lane.
@@ -450,6 +475,10 @@ __device__ __forceinline__ UnitPlan shfl_plan(const UnitPlan& p, int src) {
   q.gd = __shfl_sync(F, p.gd, src);
   q.tn = __shfl_sync(F, p.tn, src);
   q.dn = __shfl_sync(F, p.dn, src);
+  q.thoff = __shfl_sync(F, p.thoff, src);
+  q.dhoff = __shfl_sync(F, p.dhoff, src);
+  q.len = __shfl_sync(F, p.len, src);
+  q.v0 = __shfl_sync(F, p.v0, src);
   q.ts = reinterpret_cast<const unsigned char*>(
       __shfl_sync(F, reinterpret_cast<unsigned long long>(p.ts), src));
   q.ds = reinterpret_cast<const unsigned char*>(
@@ -473,6 +502,12 @@ __device__ __forceinline__ void issue_unit(const Params& P, const RowsSmem& sm, 
   info->gd = p.gd;
   info->x = -1;
   info->ell = 0;
+  info->tn = p.tn;
+  info->dn = p.dn;
+  info->thoff = p.thoff;
+  info->dhoff = p.dhoff;
+  info->len = p.len;
+  info->v0 = p.v0;
   const uint32_t bar = sm.full(s);
   mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tn + p.dn));
   if (p.tn) bulk_g2s(smem_addr(sm.tbuf(s)), p.ts, p.tn, bar);
@@ -552,13 +587,13 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
     // group on its own stream of units.  Labels off: all run pass 1.
     if (warp < NW1) {
       const int ct = tid;
-      for (int32_t i = 0; i < n_units; ++i) {  // pass 1 of unit i
-        const int s = i % NS;
-        mbar_wait(sm.full(s), (i / NS) & 1, timeout);
+      RingPos rp{0, 0u};
+      for (int32_t i = 0; i < n_units; ++i, rp.next(NS)) {  // pass 1 of unit i
+        const int s = rp.idx;
+        mbar_wait(sm.full(s), rp.par, timeout);
         const RowInfo info = *sm.info(s);
         bool bad = false;
-        const Slice s_t = target_slice<ES>(P, info);
-        const Slice s_d = draft_slice<ES>(P, info);
+        const Slice s_t = slice_t(info), s_d = slice_d(info);
         RStat a_t, a_d;
         const bool fast = !TRACK && NEED_Z && info.pair && slice_aligned<ES>(s_t) &&
                           slice_aligned<ES>(s_d) &&
@@ -582,16 +617,16 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
       }
     } else {
       const int ct = tid - NT1;
-      for (int32_t j = 0; j < n_units; ++j) {  // pass 2 of unit j, then release its stage
-        const int s = j % NS;
-        mbar_wait(sm.full(s), (j / NS) & 1, timeout);
+      RingPos rp{0, 0u};
+      for (int32_t j = 0; j < n_units; ++j, rp.next(NS)) {  // pass 2 of unit j, then release its stage
+        const int s = rp.idx;
+        mbar_wait(sm.full(s), rp.par, timeout);
         const RowInfo info = *sm.info(s);
         if (info.pair) {
-          mbar_wait(sm.statsbar(s), (j / NS) & 1, timeout);
+          mbar_wait(sm.statsbar(s), rp.par, timeout);
           const float* st = sm.stats(s);
           const float ht = st[0], hd = st[4], delta = st[6];
-          const Slice s_t = target_slice<ES>(P, info);
-          const Slice s_d = draft_slice<ES>(P, info);
+          const Slice s_t = slice_t(info), s_d = slice_d(info);
           float part;
           if (slice_aligned<ES>(s_t) && slice_aligned<ES>(s_d)) {
             // k_d = h_d + delta as hi + lo (two-sum, exact)
@@ -619,14 +654,15 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
     // After unit j releases stage s: write unit j's label partial and issue
     // unit j + NS into the stage.  Plans for the next 32 units are made
     // (all lanes, one unit each) before waiting, off the refill's path.
-    for (int32_t j = 0; j < n_units; ++j) {
-      const int s = j % NS;
+    RingPos rp{0, 0u};
+    for (int32_t j = 0; j < n_units; ++j, rp.next(NS)) {
+      const int s = rp.idx;
       const int32_t nxt = j + NS;
       if (nxt < n_units && nxt >= plan_base + 32) {
         plan_base += 32;
         if (plan_base + lane < n_units) plan = plan_unit<ES>(P, offs, c + (plan_base + lane) * N);
       }
-      mbar_wait(sm.empty(s), (j / NS) & 1, timeout);
+      mbar_wait(sm.empty(s), rp.par, timeout);
       const UnitPlan q = shfl_plan(plan, (nxt - plan_base) & 31);
       if (lane == 0) {
         const RowInfo* pj = sm.info(s);
@@ -643,10 +679,13 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
     }
   } else if (warp < W_GATH) {
     // =============================== publisher warps (unit i by warp i % kPublishers)
+    RingPos rp{0, 0u};
+    for (int w = 0; w < warp - W_PUB; ++w) rp.next(NS);
     for (int32_t i = warp - W_PUB; i < n_units; i += kPublishers) {
-      const int s = i % NS;
-      mbar_wait(sm.partbar(s), (i / NS) & 1, timeout);
-      mbar_wait(sm.full(s), (i / NS) & 1, timeout);
+      const int s = rp.idx;
+      mbar_wait(sm.partbar(s), rp.par, timeout);
+      mbar_wait(sm.full(s), rp.par, timeout);
+      for (int w = 0; w < kPublishers; ++w) rp.next(NS);
       const RowInfo info = *sm.info(s);
       RStat b_t = rstat_empty(), b_d = rstat_empty();
       int flags = 0;
@@ -658,12 +697,12 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
       }
       rstat_warp_reduce2<TRACK>(b_t, b_d);
       flags = __reduce_or_sync(0xffffffffu, flags);
-      const Slice s_t = target_slice<ES>(P, info);
+      const Slice s_t = slice_t(info);
       const bool hasx = info.pair && info.x >= s_t.v0 && info.x < s_t.v0 + s_t.len;
       float xt = 0.f, xd = 0.f;
       if (hasx) {
         xt = slice_elem<ES>(sm.tbuf(s), s_t, info.x - s_t.v0);
-        xd = slice_elem<ES>(sm.dbuf(s), draft_slice<ES>(P, info), info.x - s_t.v0);
+        xd = slice_elem<ES>(sm.dbuf(s), slice_d(info), info.x - s_t.v0);
       }
       // lane w < R_NWORDS publishes word w of the partial, tagged (selects,
       // no divergent branches)
@@ -689,13 +728,17 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
   } else {
     // =============================== gatherer warps (unit j by warp j % kGatherers)
     const int q = warp - W_GATH;
+    RingPos rp{0, 0u};
+    for (int w = 0; w < q; ++w) rp.next(NS);
     for (int32_t j = q; j < n_units; j += kGatherers) {
-      const int s = j % NS;
-      mbar_wait(sm.full(s), (j / NS) & 1, timeout);
+      const int s = rp.idx;
+      const uint32_t par = rp.par;
+      for (int w = 0; w < kGatherers; ++w) rp.next(NS);
+      mbar_wait(sm.full(s), par, timeout);
       const RowInfo info = *sm.info(s);
       // start polling once this CTA has finished pass 1 of the unit (the
       // other slices of the row are handled in the same round elsewhere)
-      mbar_wait(sm.partbar(s), (j / NS) & 1, timeout);
+      mbar_wait(sm.partbar(s), par, timeout);
       // wait until the S partials of this row carry this call's tag (lane =
       // slice): poll one word per slice, then read all words and check each
       const uint64_t* row_parts = parts + static_cast<size_t>(info.g) * kMaxSlices * kPartWords;
