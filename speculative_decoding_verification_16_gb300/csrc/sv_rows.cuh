@@ -489,9 +489,16 @@ __device__ __forceinline__ UnitPlan shfl_plan(const UnitPlan& p, int src) {
 // Producer step (one lane): load the planned unit into stage s.  The stage's
 // `full` barrier completes when the bulk copies' bytes have landed and the
 // row metadata copied by cp.async has arrived.
-template <int ES>
 __device__ __forceinline__ void issue_unit(const Params& P, const RowsSmem& sm, const UnitPlan& p,
                                            int s) {
+  // the bulk copies go out first; the stage's `full` barrier completes once
+  // their bytes have landed and three arrivals have happened: this
+  // expect_tx, the plain arrival that releases the RowInfo writes, and the
+  // completion of the cp.async copies of the row's token, length and uniform
+  const uint32_t bar = sm.full(s);
+  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tn + p.dn));
+  if (p.tn) bulk_g2s(smem_addr(sm.tbuf(s)), p.ts, p.tn, bar);
+  if (p.dn) bulk_g2s(smem_addr(sm.dbuf(s)), p.ds, p.dn, bar);
   RowInfo* info = sm.info(s);
   info->g = p.g;
   info->k = p.k;
@@ -508,10 +515,7 @@ __device__ __forceinline__ void issue_unit(const Params& P, const RowsSmem& sm, 
   info->dhoff = p.dhoff;
   info->len = p.len;
   info->v0 = p.v0;
-  const uint32_t bar = sm.full(s);
-  mbar_arrive_expect_tx(bar, static_cast<uint32_t>(p.tn + p.dn));
-  if (p.tn) bulk_g2s(smem_addr(sm.tbuf(s)), p.ts, p.tn, bar);
-  if (p.dn) bulk_g2s(smem_addr(sm.dbuf(s)), p.ds, p.dn, bar);
+  mbar_arrive(bar);
   cp_async4(smem_addr(&info->u), P.uniforms + p.g);
   cp_async4(smem_addr(&info->ell), P.lens + p.r);
   if (p.pair) cp_async4(smem_addr(&info->x), P.draft_tokens + p.gd);
@@ -526,6 +530,10 @@ __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
 
 __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // Threads of the rows kernel: NCW consumer warps, producer, publishers, gatherers.
@@ -565,8 +573,9 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
   if (warp == W_PROD) {
     if (lane == 0) {
       for (int s = 0; s < NS; ++s) {
-        mbar_init(sm.full(s), 2);                 // bulk-copy arm + cp.async completion
-        mbar_init(sm.empty(s), (NEED_CONF ? NW2 : NW1) + 2);  // + publisher + gatherer
+        mbar_init(sm.full(s), 3);  // bulk-copy arm, RowInfo release, cp.async completion
+        // pass-1 warps (labels off) or the pass-2 group, + publisher + gatherer
+        mbar_init(sm.empty(s), (NEED_CONF ? 1 : NW1) + 2);
         mbar_init(sm.partbar(s), NW1);
         mbar_init(sm.statsbar(s), 1);
       }
@@ -575,7 +584,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
     if (lane < n_units) plan = plan_unit<ES>(P, offs, c + lane * N);
     for (int i = 0; i < NS && i < n_units; ++i) {
       const UnitPlan q = shfl_plan(plan, i);
-      if (lane == 0) issue_unit<ES>(P, sm, q, i);
+      if (lane == 0) issue_unit(P, sm, q, i);
     }
   }
   __syncthreads();
@@ -645,15 +654,25 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
           part = warp_sum_f32(part);
           if (lane == 0) sm.cp(s)[warp - NW1] = part;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sm.empty(s));
+        // the whole group is done with the stage; its first warp writes the
+        // unit's label partial (warp partials summed in order) and releases
+        // the stage
+        named_bar_sync(1, NT2);
+        if (warp == NW1 && lane == 0) {
+          if (info.pair) {
+            float cs = 0.f;
+            for (int w = 0; w < NW2; ++w) cs += sm.cp(s)[w];
+            P.cpart[static_cast<size_t>(info.g) * kMaxSlices + info.k] = cs / sm.stats(s)[1];
+          }
+          mbar_arrive(sm.empty(s));
+        }
       }
     }
   } else if (warp == W_PROD) {
     // =============================== producer warp
-    // After unit j releases stage s: write unit j's label partial and issue
-    // unit j + NS into the stage.  Plans for the next 32 units are made
-    // (all lanes, one unit each) before waiting, off the refill's path.
+    // After unit j releases stage s, issue unit j + NS into it.  Plans for
+    // the next 32 units are made (all lanes, one unit each) before waiting,
+    // off the refill's path.
     RingPos rp{0, 0u};
     for (int32_t j = 0; j < n_units; ++j, rp.next(NS)) {
       const int s = rp.idx;
@@ -664,17 +683,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
       }
       mbar_wait(sm.empty(s), rp.par, timeout);
       const UnitPlan q = shfl_plan(plan, (nxt - plan_base) & 31);
-      if (lane == 0) {
-        const RowInfo* pj = sm.info(s);
-        const int32_t pg = pj->g, pk = pj->k, ppair = pj->pair;
-        float cs = 0.f, z = 1.f;
-        if (NEED_CONF && ppair) {  // label partial of unit j (read before the refill)
-          for (int w = 0; w < NW2; ++w) cs += sm.cp(s)[w];
-          z = sm.stats(s)[1];
-        }
-        if (nxt < n_units) issue_unit<ES>(P, sm, q, s);
-        if (NEED_CONF && ppair) P.cpart[static_cast<size_t>(pg) * kMaxSlices + pk] = cs / z;
-      }
+      if (lane == 0 && nxt < n_units) issue_unit(P, sm, q, s);
       __syncwarp();
     }
   } else if (warp < W_GATH) {
