@@ -35,7 +35,11 @@ struct ReqInfo {
   int32_t ok, off, ell, a, residual, pad[3];
 };
 
-__device__ __forceinline__ ReqInfo scan_request(const Params& P, int32_t r) {
+// Request r's layout and its first rejected position a_r, by one warp (every
+// lane gets the result): lane j looks at drafted position j, so the accept
+// flags are read in one round of independent loads instead of a dependent
+// chain of l_r - 1.
+__device__ __forceinline__ ReqInfo scan_request(const Params& P, int32_t r, int lane) {
   ReqInfo q{};
   const int32_t off = __ldg(P.offs + r), off1 = __ldg(P.offs + r + 1), ell = __ldg(P.lens + r);
   q.ok = ell >= 1 && ell <= P.max_len && off1 - off == ell && off >= r && off1 <= P.Nt &&
@@ -43,8 +47,18 @@ __device__ __forceinline__ ReqInfo scan_request(const Params& P, int32_t r) {
   q.off = off;
   q.ell = ell;
   int32_t a = 0;
-  if (q.ok)
-    while (a < ell - 1 && P.rec[off + a].acc) ++a;
+  if (q.ok) {
+    a = ell - 1;  // every drafted token accepted
+    for (int32_t base = 0; base < ell - 1; base += 32) {
+      const int32_t j = base + lane;
+      const bool rejected = j < ell - 1 && !P.rec[off + j].acc;
+      const unsigned m = __ballot_sync(0xffffffffu, rejected);
+      if (m) {
+        a = base + __ffs(m) - 1;
+        break;
+      }
+    }
+  }
   q.a = a;
   q.residual = a < ell - 1;
   // the draft partner of the stopping row must exist (guards corrupt offsets)
@@ -125,10 +139,13 @@ __global__ void __launch_bounds__(kThreads) finalize_draw_kernel(const Params P)
   const uint32_t bar = smem_addr(smem + kF_OffBars);
 
   cluster_arrive_relaxed();
-  if (tid == 0) {
-    *sinfo = scan_request(P, r);
-    mbar_init(bar, 1);
-    fence_mbar_init();
+  if (tid < 32) {
+    const ReqInfo rq = scan_request(P, r, tid);
+    if (tid == 0) {
+      *sinfo = rq;
+      mbar_init(bar, 1);
+      fence_mbar_init();
+    }
   }
   __syncthreads();
   const ReqInfo q = *sinfo;
@@ -253,15 +270,16 @@ __global__ void __launch_bounds__(kThreads) finalize_draw_kernel(const Params P)
     break;
   }
 
-  if (rank == 0 && tid == 0) {
-    P.out_accept_len[r] = q.a;
-    for (int32_t j = 0; j < q.ell; ++j) {
+  if (rank == 0 && tid < 32) {  // accepted drafts, -1 after the final token, flags
+    if (tid == 0) P.out_accept_len[r] = q.a;
+    int flags = 0;
+    for (int32_t j = tid; j < q.ell; j += 32) {
       if (j < q.a) P.out_tokens[q.off + j] = __ldg(P.draft_tokens + q.off - r + j);
       else if (j > q.a) P.out_tokens[q.off + j] = -1;
+      if (j <= q.a) flags |= P.rec[q.off + j].flags;
     }
-    int flags = any_timeout ? SV_DEVERR_TIMEOUT : 0;
-    for (int32_t j = 0; j <= q.a && j < q.ell; ++j) flags |= P.rec[q.off + j].flags;
-    if (flags) raise_error(P, flags);
+    flags = __reduce_or_sync(0xffffffffu, flags) | (any_timeout ? SV_DEVERR_TIMEOUT : 0);
+    if (tid == 0 && flags) raise_error(P, flags);
   }
   if (any_timeout) {  // one more bounded wait for a copy still in flight
     bool again = false;
@@ -274,26 +292,26 @@ __global__ void __launch_bounds__(kThreads) finalize_draw_kernel(const Params P)
 __global__ void __launch_bounds__(kThreads) finalize_select_kernel(const Params P) {
   const int32_t r = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (r >= P.B) return;
-  const ReqInfo q = scan_request(P, r);
+  if (r >= P.B) return;  // whole warps leave together
+  const ReqInfo q = scan_request(P, r, lane);
   if (!q.ok) {
     if (lane == 0) raise_error(P, SV_DEVERR_LEN);
     return;
   }
   sum_labels(P, r, q.off, q.ell, lane);
-  if (lane != 0) return;
   const RowRec& fr = P.rec[q.off + q.a];
   const int32_t final_tok = P.mode == SV_GREEDY ? fr.argt : fr.pick;
-  P.out_accept_len[r] = q.a;
+  if (lane == 0) P.out_accept_len[r] = q.a;
   int flags = 0;
-  for (int32_t j = 0; j < q.ell; ++j) {
+  for (int32_t j = lane; j < q.ell; j += 32) {
     int32_t v = -1;
     if (j < q.a) v = __ldg(P.draft_tokens + q.off - r + j);
     else if (j == q.a) v = final_tok;
     P.out_tokens[q.off + j] = v;
     if (j <= q.a) flags |= P.rec[q.off + j].flags;
   }
-  if (flags) raise_error(P, flags);
+  flags = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0 && flags) raise_error(P, flags);
 }
 
 }  // namespace sv
