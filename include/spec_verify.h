@@ -184,7 +184,7 @@ int spec_verify_finalize(const void* target_logits, const void* draft_logits,
  * convenience, and computes exactly what spec_verify computes.
  *
  * Scratch is a file-scope device array of this library sized for
- * SV_STATIC_MAX_ROWS target rows (about 17.4 MB of device memory, reserved
+ * SV_STATIC_MAX_ROWS target rows (about 21.9 MB of device memory, reserved
  * when the library's module is loaded on a device).  Nothing is allocated by
  * the call.  n_target_rows > SV_STATIC_MAX_ROWS returns SV_ERR_TOO_LARGE
  * before anything is enqueued.

@@ -16,6 +16,7 @@
 
 #include "spec_verify.h"
 #include "sv_common.cuh"
+#include "sv_filter.cuh"
 #include "sv_finalize.cuh"
 #include "sv_rows.cuh"
 
@@ -61,8 +62,14 @@ int rowbuf_bytes(int S, int es) { return round_up(S * es + 32, 128); }
 
 int slice_len(int V, int C, int es) { return round_up((V + C - 1) / C, 16 / es); }
 
-bool is_filtered(int V, int top_k, float top_p) {
-  return (top_k > 0 && top_k < V) || top_p < 1.0f;
+// Size k of the kept set under top-k / top-p filtering: 0 when unfiltered,
+// -1 when the set can exceed SV_MAX_FILTER_K tokens (not served).
+int filter_k(int V, int top_k, float top_p) {
+  const bool use_k = top_k > 0 && top_k < V;
+  const bool use_p = top_p < 1.0f;
+  if (!use_k && !use_p) return 0;
+  const int k = use_k ? top_k : V;
+  return k <= SV_MAX_FILTER_K ? k : -1;
 }
 
 // Geometry of the rows kernel: a row is cut into S <= kMaxSlices slices of
@@ -234,12 +241,14 @@ int check_args(const Args& a) {
   if (a.workspace == nullptr || !aligned(a.workspace, 256) ||
       a.workspace_bytes < spec_verify_workspace_size(a.B, a.n_target_rows))
     return SV_ERR_WORKSPACE;
-  if (is_filtered(a.V, a.top_k, a.top_p)) return SV_ERR_UNSUPPORTED;  // served by a later kernel
+  if (filter_k(a.V, a.top_k, a.top_p) < 0) return SV_ERR_UNSUPPORTED;
   return SV_OK;
 }
 
 // Workspace layout: RowRec[N_t] | label partials float[N_t][32] | published
-// pass-1 partials uint64[N_t][32][16] (tag in the upper half of every word).
+// pass-1 partials uint64[N_t][32][16] (tag in the upper half of every word) |
+// filtered-path row records FiltRow[2 N_t] (N_t target rows, then the draft
+// rows).
 size_t ws_cpart_offset(int32_t n_target_rows) {
   return (static_cast<size_t>(n_target_rows) * sizeof(RowRec) + 255) / 256 * 256;
 }
@@ -247,6 +256,11 @@ size_t ws_cpart_offset(int32_t n_target_rows) {
 size_t ws_parts_offset(int32_t n_target_rows) {
   return ws_cpart_offset(n_target_rows) +
          (static_cast<size_t>(n_target_rows) * kMaxSlices * sizeof(float) + 255) / 256 * 256;
+}
+
+size_t ws_filt_offset(int32_t n_target_rows) {
+  return ws_parts_offset(n_target_rows) +
+         static_cast<size_t>(n_target_rows) * kMaxSlices * kPartWords * 8;
 }
 
 Params make_params(const Args& a) {
@@ -265,7 +279,7 @@ Params make_params(const Args& a) {
   const bool need_t = a.mode == SV_SAMPLE || a.out_conf != nullptr || a.out_row_stats != nullptr;
   P.T = need_t ? a.temperature : 1.f;
   P.sc = static_cast<float>(1.4426950408889634 / static_cast<double>(P.T));
-  P.top_k = (a.top_k > 0 && a.top_k < a.V) ? a.top_k : 0;
+  P.top_k = std::max(0, filter_k(a.V, a.top_k, a.top_p));  // > 0: filtered path
   P.top_p = a.top_p;
   P.mode = a.mode;
   P.out_tokens = a.out_tokens;
@@ -277,6 +291,7 @@ Params make_params(const Args& a) {
   P.cpart = reinterpret_cast<float*>(static_cast<unsigned char*>(a.workspace) +
                                      ws_cpart_offset(a.n_target_rows));
   P.parts = static_cast<unsigned char*>(a.workspace) + ws_parts_offset(a.n_target_rows);
+  P.filt = static_cast<unsigned char*>(a.workspace) + ws_filt_offset(a.n_target_rows);
   return P;
 }
 
@@ -342,6 +357,14 @@ int run_rows(const Args& a) {
   if (rc != SV_OK) return rc;
   Params P = make_params(a);
   const int es = a.dtype == SV_BF16 ? 2 : 4;
+  cudaStream_t st = static_cast<cudaStream_t>(a.stream);
+  if (P.top_k > 0) {  // top-k / top-p: one streaming pass per row, no exchange
+    const int rows = P.Nt + P.Nd;
+    const int grid = std::max(1, std::min(rows, dc.sms * kFilterCtasPerSm));
+    if (es == 2) filter_rows_kernel<2><<<grid, kThreads, 0, st>>>(P);
+    else filter_rows_kernel<4><<<grid, kThreads, 0, st>>>(P);
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  }
   RowsGeom geo;
   rc = rows_geometry(a.V, a.B, es, dc, &geo);
   if (rc != SV_OK) return rc;
@@ -363,7 +386,6 @@ int run_rows(const Args& a) {
   // (SPEC_VERIFY_WARPS, SPEC_VERIFY_PASS1_WARPS)
   const int ncw = env_int("SPEC_VERIFY_WARPS", 16) >= 24 ? 24 : 16;
   P.nw1 = std::max(1, std::min(ncw - 1, env_int("SPEC_VERIFY_PASS1_WARPS", ncw / 2)));
-  cudaStream_t st = static_cast<cudaStream_t>(a.stream);
   if (es == 2)
     return ncw == 24 ? launch_rows<2, 24>(P, smem, dc, need_z, need_conf, track, st)
                      : launch_rows<2, 16>(P, smem, dc, need_z, need_conf, track, st);
@@ -377,13 +399,16 @@ int run_finalize(const Args& a) {
   if (rc != SV_OK) return rc;
   Params P = make_params(a);
   const int es = a.dtype == SV_BF16 ? 2 : 4;
+  cudaStream_t st = static_cast<cudaStream_t>(a.stream);
+  if (P.top_k > 0) {  // top-k / top-p: decisions on the kept sets, one warp per request
+    filter_requests_kernel<<<(a.B + kWarps - 1) / kWarps, kThreads, 0, st>>>(P);
+    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  }
   RowsGeom geo;
   rc = rows_geometry(a.V, a.B, es, dc, &geo);
   if (rc != SV_OK) return rc;
   P.nslices = geo.S;
-  cudaStream_t st = static_cast<cudaStream_t>(a.stream);
-  const bool filtered = P.top_k > 0 || P.top_p < 1.f;
-  if (a.mode == SV_GREEDY || filtered) {
+  if (a.mode == SV_GREEDY) {
     finalize_select_kernel<<<(a.B + kWarps - 1) / kWarps, kThreads, 0, st>>>(P);
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
   }
@@ -402,7 +427,7 @@ int run_finalize(const Args& a) {
 // ---------------------------------------------------------------- static scratch
 // Scratch of spec_verify_static: the same three workspace regions as a caller
 // workspace (row records, label partials, published pass-1 partials), sized
-// for SV_STATIC_MAX_ROWS target rows (about 17.4 MB), in a file-scope device
+// for SV_STATIC_MAX_ROWS target rows (about 21.9 MB), in a file-scope device
 // array so that the call needs no allocation.  Some callers cannot allocate
 // device memory at the point where they verify: a host loop in plain C with
 // no caching allocator, where cudaMalloc / cudaFree would synchronise the
@@ -414,7 +439,8 @@ constexpr size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 constexpr size_t kStaticBytes =
     round256(round256(static_cast<size_t>(SV_STATIC_MAX_ROWS) * sizeof(RowRec)) +
              round256(static_cast<size_t>(SV_STATIC_MAX_ROWS) * kMaxSlices * sizeof(float)) +
-             static_cast<size_t>(SV_STATIC_MAX_ROWS) * kMaxSlices * kPartWords * 8) +
+             static_cast<size_t>(SV_STATIC_MAX_ROWS) * kMaxSlices * kPartWords * 8 +
+             static_cast<size_t>(SV_STATIC_MAX_ROWS) * 2 * sizeof(FiltRow)) +
     256;
 
 __device__ __align__(256) unsigned char g_static_ws[kStaticBytes];
@@ -462,8 +488,7 @@ extern "C" {
 size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows) {
   (void)B;
   const int32_t rows = n_target_rows > 0 ? n_target_rows : 0;
-  const size_t bytes = sv::ws_parts_offset(rows) +
-                       static_cast<size_t>(rows) * sv::kMaxSlices * sv::kPartWords * 8;
+  const size_t bytes = sv::ws_filt_offset(rows) + static_cast<size_t>(rows) * 2 * sizeof(sv::FiltRow);
   return (bytes + 255) / 256 * 256 + 256;
 }
 

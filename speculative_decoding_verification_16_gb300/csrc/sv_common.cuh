@@ -49,6 +49,7 @@ struct Params {
   RowRec* rec;
   float* cpart;      // [N_t][32] label partial of each (row, slice) unit
   void* parts;       // [N_t][32][16] words: published pass-1 partials
+  void* filt;        // filtered path: FiltRow per target row, then per draft row
   uint32_t tag;      // per-call tag of the published partials (never 0)
   int32_t nslices;   // slices per row of the rows kernel (<= 32)
   int32_t nunits;    // N_t * nslices

@@ -1,0 +1,421 @@
+// sv_filter.cuh -- the verify step with top-k (k <= 64) and top-p filtering.
+//
+// Sampling parameters temperature, top_k and top_p (DSpine page, "加速效果":
+// T 1.0, top_p 0.95, top_k 20) apply to the target and the draft rows alike.
+// Every probability the verify step needs is then supported on at most k
+// tokens per row, so the work splits in two:
+//
+//  filter_rows_kernel   one CTA per logits row, one streaming pass: the row's
+//                       k largest logits by (value desc, id asc), exact; then
+//                       the softmax weights of those k relative to the row
+//                       maximum, renormalised, and the top-p cut (shortest
+//                       prefix of that order whose cumulative probability
+//                       reaches top_p), renormalised again.  The kept tokens
+//                       and weights go to a FiltRow record in the workspace.
+//  filter_requests_kernel  one warp per request, on the FiltRow records only:
+//                       the accept chain u * p_d(x) < p_t(x) (greedy: x is
+//                       the target argmax), the confidence labels
+//                       c* = sum_v min(p_t, p_d) over the two kept sets
+//                       (DSpark tutorial, "置信度预测头"), and the final token:
+//                       an inverse-CDF draw over ascending ids from
+//                       max(0, p_t - p_d) of the rejected pair, or from p_t
+//                       of the bonus row (DFlash / Spec V2 page, A3; DSpark
+//                       tutorial, "推测解码的两步流程").
+//
+// Selection keys: a logit's float bits mapped to an unsigned key that orders
+// like the value, in the upper 32 bits, and the complement of the token id in
+// the lower 32, so that a larger key means a larger logit or, for equal
+// logits, a smaller id.  Keys are unique, so the selected set does not depend
+// on the order in which the row is read.
+#pragma once
+
+#include "sv_common.cuh"
+
+namespace sv {
+
+constexpr int kMaxK = SV_MAX_FILTER_K;  // 64
+constexpr int kCandCap = 2 * kMaxK;     // per-warp candidate buffer
+constexpr int kFilterCtasPerSm = 4;
+
+struct FiltRow {
+  int32_t n;       // kept tokens (<= k)
+  int32_t argmax;  // lowest id holding the row maximum
+  float h;         // reference: x_max * sc
+  float z;         // sum of the kept weights
+  float xmax;      // row maximum (raw logit)
+  int32_t flags;   // device error bits of this row
+  int32_t pad[2];
+  int32_t ids[kMaxK];  // kept tokens, by (value desc, id asc)
+  float w[kMaxK];      // their weights exp2(x sc - h); p = w / z
+};
+static_assert(sizeof(FiltRow) == 544, "FiltRow layout");
+
+__device__ __forceinline__ uint32_t order_key(float x) {
+  const uint32_t u = __float_as_uint(x);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint64_t c) {
+  const uint32_t k = static_cast<uint32_t>(c >> 32);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ __forceinline__ int32_t key_id(uint64_t c) {
+  return static_cast<int32_t>(~static_cast<uint32_t>(c));
+}
+
+// Sort n (a power of two, <= 2 * 32 * per) keys of a warp's shared buffer in
+// descending order (bitonic network; entries >= count must already be 0).
+__device__ __forceinline__ void warp_sort_desc(uint64_t* a, int n) {
+  const int lane = threadIdx.x & 31;
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      __syncwarp();
+      for (int i = lane; i < n; i += 32) {
+        const int p = i ^ j;
+        if (p > i) {
+          const uint64_t x = a[i], y = a[p];
+          const bool desc = (i & k) == 0;
+          if (desc ? (x < y) : (x > y)) {
+            a[i] = y;
+            a[p] = x;
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+// Keep the kmax largest keys of a warp's buffer (sorted, descending) and
+// return the new count; entries beyond it are cleared.
+__device__ __forceinline__ int warp_prune(uint64_t* cand, int cnt, int kmax) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  for (int i = cnt + lane; i < kCandCap; i += 32) cand[i] = 0;
+  warp_sort_desc(cand, kCandCap);
+  const int keep = min(cnt, kmax);
+  for (int i = keep + lane; i < kCandCap; i += 32) cand[i] = 0;
+  __syncwarp();
+  return keep;
+}
+
+// 16-byte read-only load that does not allocate in L1.
+__device__ __forceinline__ uint4 ldg_nc_v4(const unsigned char* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel(const Params P) {
+  constexpr int VEC = 16 / ES;
+  constexpr int UNROLL = 4;
+  __shared__ uint64_t cand[kWarps][kCandCap];
+  __shared__ uint64_t merged[kWarps * kMaxK];
+  __shared__ int bad_any;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  const int K = P.top_k;
+  FiltRow* recs = reinterpret_cast<FiltRow*>(P.filt);
+  const int32_t nrows = P.Nt + P.Nd;
+
+  for (int32_t row = blockIdx.x; row < nrows; row += gridDim.x) {
+    const bool is_t = row < P.Nt;
+    const unsigned char* base =
+        is_t ? P.tgt + static_cast<size_t>(row) * P.V * ES
+             : P.drf + static_cast<size_t>(row - P.Nt) * P.V * ES;
+    const Slice s = make_slice<ES>(base, P.V, 0, P.V);  // the whole row
+    const int32_t nv = s.nbytes >> 4;
+    uint64_t* my = cand[warp];
+    for (int i = lane; i < kCandCap; i += 32) my[i] = 0;
+    if (tid == 0) bad_any = 0;
+    __syncthreads();
+    int cnt = 0;        // warp-uniform
+    uint64_t thr = 0;   // warp-uniform: only larger keys can still make the top k
+    bool bad = false;
+    // the loop runs on the warp's first vector, so that every lane takes
+    // part in the warp-wide votes below; lanes past the end hold no element
+    for (int32_t kw = warp * 32; kw < nv; kw += UNROLL * kThreads) {
+      uint4 raw[UNROLL];
+#pragma unroll
+      for (int q = 0; q < UNROLL; ++q) {
+        const int32_t k = kw + lane + q * kThreads;
+        raw[q] = k < nv ? ldg_nc_v4(s.gsrc + 16 * static_cast<size_t>(k)) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int q = 0; q < UNROLL; ++q) {
+        const int32_t k = kw + lane + q * kThreads;
+        if (kw + q * kThreads >= nv) break;  // warp-uniform
+        float x[VEC];
+        const uint32_t wv[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+#pragma unroll
+        for (int l = 0; l < VEC; ++l)
+          x[l] = ES == 2 ? ((l & 1) ? bf16hi(wv[l >> 1]) : bf16lo(wv[l >> 1]))
+                         : __uint_as_float(wv[l]);
+        const int32_t i0 = k * VEC - s.hoff;
+#pragma unroll
+        for (int l = 0; l < VEC; ++l) {
+          const int32_t id = i0 + l;
+          const bool valid = k < nv && id >= 0 && id < s.len;
+          if (valid && (x[l] != x[l] || x[l] == INFINITY)) bad = true;
+          const uint64_t key =
+              valid && !(x[l] != x[l])
+                  ? (static_cast<uint64_t>(order_key(x[l])) << 32) | static_cast<uint32_t>(~id)
+                  : 0ull;
+          bool take = key > thr;
+          unsigned m = __ballot_sync(0xffffffffu, take);
+          if (!m) continue;
+          if (cnt + __popc(m) > kCandCap) {  // full: keep the best K, raise the bar
+            cnt = warp_prune(my, cnt, K);
+            thr = cnt >= K ? my[K - 1] : 0ull;
+            take = key > thr;
+            m = __ballot_sync(0xffffffffu, take);
+          }
+          if (take) my[cnt + __popc(m & lt_mask)] = key;
+          cnt += __popc(m);
+        }
+      }
+    }
+    cnt = warp_prune(my, cnt, K);
+    for (int i = lane; i < kMaxK; i += 32) merged[warp * kMaxK + i] = i < K ? my[i] : 0ull;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&bad_any, 1);
+    __syncthreads();
+    // the CTA's best K of the warps' best K: bitonic sort of kWarps * kMaxK keys
+    constexpr int NM = kWarps * kMaxK;
+    for (int kk = 2; kk <= NM; kk <<= 1) {
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        for (int i = tid; i < NM; i += kThreads) {
+          const int p = i ^ j;
+          if (p > i) {
+            const uint64_t a = merged[i], b = merged[p];
+            const bool desc = (i & kk) == 0;
+            if (desc ? (a < b) : (a > b)) {
+              merged[i] = b;
+              merged[p] = a;
+            }
+          }
+        }
+        __syncthreads();
+      }
+    }
+    if (warp == 0) {
+      // weights of the k best relative to the maximum, then the top-p cut
+      FiltRow* fr = recs + row;
+      const float sc = P.sc;
+      const uint64_t c0 = merged[lane], c1 = merged[lane + 32];
+      const float xmax = key_value(merged[0]);
+      const float h = xmax * sc;
+      const bool v0 = lane < K && c0 != 0ull, v1 = lane + 32 < K && c1 != 0ull;
+      const float x0 = v0 ? key_value(c0) : 0.f, x1 = v1 ? key_value(c1) : 0.f;
+      const float w0 = v0 ? ex2(fmaf(x0, sc, -h)) : 0.f;
+      const float w1 = v1 ? ex2(fmaf(x1, sc, -h)) : 0.f;
+      const int navail = __popc(__ballot_sync(0xffffffffu, v0)) + __popc(__ballot_sync(0xffffffffu, v1));
+      // inclusive prefix sums in (value desc, id asc) order: entries 0..31, then 32..63
+      float p0 = w0, p1 = w1;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const float a = __shfl_up_sync(0xffffffffu, p0, off);
+        const float b = __shfl_up_sync(0xffffffffu, p1, off);
+        if (lane >= off) p0 += a, p1 += b;
+      }
+      const float half = __shfl_sync(0xffffffffu, p0, 31);
+      p1 += half;
+      const float zk = __shfl_sync(0xffffffffu, p1, 31);  // sum of the k weights
+      int n = navail;
+      if (P.top_p < 1.f) {
+        // shortest prefix whose cumulative probability reaches top_p
+        const unsigned r0 = __ballot_sync(0xffffffffu, v0 && p0 / zk >= P.top_p);
+        const unsigned r1 = __ballot_sync(0xffffffffu, v1 && p1 / zk >= P.top_p);
+        if (r0) n = __ffs(r0);
+        else if (r1) n = 32 + __ffs(r1);
+      }
+      float z = n > 32 ? __shfl_sync(0xffffffffu, p1, (n - 33) & 31)
+                       : __shfl_sync(0xffffffffu, p0, (n - 1) & 31);
+      if (n == 0) z = 0.f;
+      if (lane < n) {
+        fr->ids[lane] = key_id(c0);
+        fr->w[lane] = w0;
+      }
+      if (lane + 32 < n) {
+        fr->ids[lane + 32] = key_id(c1);
+        fr->w[lane + 32] = w1;
+      }
+      const bool row_bad = bad_any != 0 || !(xmax > -INFINITY);
+      if (lane == 0) {
+        fr->n = n;
+        fr->argmax = key_id(merged[0]);
+        fr->h = h;
+        fr->z = z;
+        fr->xmax = xmax;
+        fr->flags = row_bad ? SV_DEVERR_NAN : 0;
+        if (row_bad) raise_error(P, SV_DEVERR_NAN);
+        if (P.out_row_stats != nullptr) {
+          float* o = P.out_row_stats + 3 * static_cast<size_t>(row);  // targets, then drafts
+          o[0] = xmax / P.T;
+          o[1] = z * exp2f(h - xmax * sc);
+          o[2] = __int_as_float(key_id(merged[0]));
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// Probability of token v in a kept set held in shared memory (0 if absent).
+__device__ __forceinline__ float kept_prob(const FiltRow& r, int32_t v) {
+  for (int i = 0; i < r.n; ++i)
+    if (r.ids[i] == v) return r.w[i] / r.z;
+  return 0.f;
+}
+
+__device__ __forceinline__ void copy_row(FiltRow& dst, const FiltRow* src, int lane) {
+  const int4* s = reinterpret_cast<const int4*>(src);
+  int4* d = reinterpret_cast<int4*>(&dst);
+  for (int i = lane; i < static_cast<int>(sizeof(FiltRow) / 16); i += 32) d[i] = s[i];
+  __syncwarp();
+}
+
+// One warp per request: accept chain, labels, final token, outputs.
+__global__ void __launch_bounds__(kThreads) filter_requests_kernel(const Params P) {
+  __shared__ FiltRow rows[kWarps][2];  // target row, draft row of the current position
+  __shared__ int32_t draw_id[kWarps][kMaxK];
+  __shared__ float draw_w[kWarps][kMaxK];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int32_t r = blockIdx.x * kWarps + warp;
+  if (r >= P.B) return;  // whole warps leave together
+  const FiltRow* recs = reinterpret_cast<const FiltRow*>(P.filt);
+  FiltRow& T = rows[warp][0];
+  FiltRow& D = rows[warp][1];
+  const int32_t off = __ldg(P.offs + r), off1 = __ldg(P.offs + r + 1), ell = __ldg(P.lens + r);
+  const bool ok = ell >= 1 && ell <= P.max_len && off1 - off == ell && off >= r && off1 <= P.Nt &&
+                  (r != 0 || off == 0) && (r != P.B - 1 || off1 == P.Nt) &&
+                  off - r + ell - 1 <= P.Nd;
+  if (!ok) {
+    if (lane == 0) raise_error(P, SV_DEVERR_LEN);
+    return;
+  }
+  int flags = 0;
+  // labels of every drafted position, and the accept chain up to the first failure
+  int32_t a = ell - 1;
+  bool stopped = false;
+  for (int32_t j = 0; j < ell - 1; ++j) {
+    copy_row(T, recs + off + j, lane);
+    copy_row(D, recs + P.Nt + off - r + j, lane);
+    if (lane == 0) flags |= T.flags | D.flags;
+    const int32_t x = __ldg(P.draft_tokens + off - r + j);
+    if (P.out_conf != nullptr) {
+      float c = 0.f;
+      for (int i = lane; i < T.n; i += 32) c += fminf(T.w[i] / T.z, kept_prob(D, T.ids[i]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+      if (lane == 0) P.out_conf[off - r + j] = c;
+    }
+    if (stopped) continue;
+    bool acc;
+    if (x < 0 || x >= P.V) {
+      flags |= SV_DEVERR_TOKEN;
+      acc = false;
+    } else if (P.mode == SV_GREEDY) {
+      acc = x == T.argmax;
+    } else {
+      const float pt = kept_prob(T, x), pd = kept_prob(D, x);
+      const float u = __ldg(P.uniforms + off + j);
+      acc = pd > 0.f ? u * pd < pt : pt > 0.f;
+    }
+    if (!acc) {
+      a = j;
+      stopped = true;
+      if (P.out_conf == nullptr) break;
+    }
+  }
+  // final token from target row a (and its draft partner when a < l - 1)
+  copy_row(T, recs + off + a, lane);
+  if (lane == 0) flags |= T.flags;
+  int32_t final_tok = T.argmax;
+  if (P.mode == SV_SAMPLE) {
+    const bool residual = a < ell - 1;
+    if (residual) copy_row(D, recs + P.Nt + off - r + a, lane);
+    // weights of the kept target tokens, then sorted by id (ascending)
+    int32_t* sid = draw_id[warp];
+    float* swt = draw_w[warp];
+    float tot = 0.f;
+    for (int q = 0; q < 2; ++q) {
+      const int i = lane + 32 * q;
+      const int32_t v = i < T.n ? T.ids[i] : 0x7fffffff;
+      const float pt = i < T.n ? T.w[i] / T.z : 0.f;
+      const float w = residual ? fmaxf(0.f, pt - kept_prob(D, v)) : pt;
+      sid[i] = v;
+      swt[i] = w;
+      tot += w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    if (residual && !(tot > 0.f)) {  // no residual mass (rounding only): draw from p_t
+      tot = 0.f;
+      for (int q = 0; q < 2; ++q) {
+        const int i = lane + 32 * q;
+        swt[i] = i < T.n ? T.w[i] / T.z : 0.f;
+        tot += swt[i];
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    }
+    for (int kk = 2; kk <= kMaxK; kk <<= 1) {  // bitonic, ascending ids
+      for (int jj = kk >> 1; jj > 0; jj >>= 1) {
+        __syncwarp();
+        for (int i = lane; i < kMaxK; i += 32) {
+          const int pj = i ^ jj;
+          if (pj > i) {
+            const bool up = (i & kk) == 0;
+            if (up ? sid[i] > sid[pj] : sid[i] < sid[pj]) {
+              const int32_t ti = sid[i]; sid[i] = sid[pj]; sid[pj] = ti;
+              const float tw = swt[i]; swt[i] = swt[pj]; swt[pj] = tw;
+            }
+          }
+        }
+      }
+    }
+    __syncwarp();
+    // inverse CDF over ascending ids: first token with cumsum > u * total
+    // (lane l holds entries 2l and 2l + 1)
+    const float w0 = swt[2 * lane], w1 = swt[2 * lane + 1];
+    const float ls = w0 + w1;
+    float incl = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const float c0 = incl - ls + w0, c1 = incl;
+    const float target = __ldg(P.uniforms + off + ell - 1) * tot;
+    const bool h0 = w0 > 0.f && c0 > target, h1 = w1 > 0.f && c1 > target;
+    const unsigned hit = __ballot_sync(0xffffffffu, h0 || h1);
+    const unsigned pos = __ballot_sync(0xffffffffu, w0 > 0.f || w1 > 0.f);
+    int e = -1;
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      e = 2 * L + (__shfl_sync(0xffffffffu, h0, L) ? 0 : 1);
+    } else if (pos) {  // rounding: the last token with mass
+      const int L = 31 - __clz(pos);
+      e = 2 * L + (__shfl_sync(0xffffffffu, w1 > 0.f, L) ? 1 : 0);
+    }
+    if (e >= 0) final_tok = sid[e];
+    else flags |= SV_DEVERR_NAN;
+  }
+  for (int32_t j = lane; j < ell; j += 32) {
+    int32_t v = -1;
+    if (j < a) v = __ldg(P.draft_tokens + off - r + j);
+    else if (j == a) v = final_tok;
+    P.out_tokens[off + j] = v;
+  }
+  flags = __reduce_or_sync(0xffffffffu, flags);
+  if (lane == 0) {
+    P.out_accept_len[r] = a;
+    if (flags) raise_error(P, flags);
+  }
+}
+
+}  // namespace sv

@@ -49,14 +49,20 @@ def compare(w, out, ref, *, check_stats=False, check_conf=True):
     for r, o in ref.items():
         off, ell = int(offs[r]), int(lens[r])
         doff = off - r
+        # a top-p cut within 1e-6 of top_p may keep one token more or less on
+        # either side: such rows' Z and labels are not compared
+        tie_t, tie_d = o["topp_near_tie_t"], o["topp_near_tie_d"]
         if conf is not None and ell > 1:
-            np.testing.assert_allclose(conf[doff:doff + ell - 1], o["conf"], rtol=0,
+            keep = [j for j in range(ell - 1) if not (tie_t[j] or tie_d[j])]
+            np.testing.assert_allclose(conf[doff:doff + ell - 1][keep], o["conf"][keep], rtol=0,
                                        atol=CONF_ATOL, err_msg=f"conf of request {r}")
         if stats is not None:
             for j in range(ell):
-                _check_stat(stats[off + j], o["stats_t"][j], f"target row {off + j}")
+                _check_stat(stats[off + j], o["stats_t"][j], f"target row {off + j}",
+                            check_z=not tie_t[j])
             for j in range(ell - 1):
-                _check_stat(stats[Nt + doff + j], o["stats_d"][j], f"draft row {doff + j}")
+                _check_stat(stats[Nt + doff + j], o["stats_d"][j], f"draft row {doff + j}",
+                            check_z=not tie_d[j])
         if o["near_tie"]:
             n_tie += 1
             continue
@@ -66,8 +72,9 @@ def compare(w, out, ref, *, check_stats=False, check_conf=True):
     return len(ref), n_tie
 
 
-def _check_stat(got, want, what):
+def _check_stat(got, want, what, check_z=True):
     m, Z, am = want
     assert int(np.float32(got[2]).view(np.int32)) == am, f"argmax of {what}"
     assert abs(got[0] - m) <= NORM_RTOL * max(1.0, abs(m)), f"m of {what}: {got[0]} vs {m}"
-    assert abs(got[1] - Z) <= NORM_RTOL * abs(Z), f"Z of {what}: {got[1]} vs {Z}"
+    if check_z:
+        assert abs(got[1] - Z) <= NORM_RTOL * abs(Z), f"Z of {what}: {got[1]} vs {Z}"

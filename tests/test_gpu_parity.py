@@ -165,8 +165,6 @@ def test_greedy_without_labels_or_stats(cuda_lib):
 def test_hand_derived_cases_on_gpu(cuda_lib):
     path = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
     for case in json.load(open(path))["cases"]:
-        if case["top_k"] or case["top_p"] < 1:
-            continue  # filtered cases are covered by the filtered-kernel tests
         rows = lambda rs: torch.tensor([[float(v) for v in r] for r in rs],  # noqa: E731
                                        dtype=torch.float32, device=DEV)
         t = rows(case["target"])
@@ -175,8 +173,8 @@ def test_hand_derived_cases_on_gpu(cuda_lib):
         w = _pair_workload(t, d, torch.tensor(case["draft_tokens"], device=DEV),
                            case["verify_lens"], torch.tensor(case["uniforms"], device=DEV),
                            mode=mode)
-        out = cuda_lib.verify_workload(w, temperature=case["temperature"], top_k=0, top_p=1.0,
-                                       max_len=16)
+        out = cuda_lib.verify_workload(w, temperature=case["temperature"], top_k=case["top_k"],
+                                       top_p=case["top_p"], max_len=16)
         torch.cuda.synchronize()
         assert out.tokens.cpu().tolist() == case["tokens"], case["name"]
         assert out.accept_len.cpu().tolist() == case["accept_len_expected"], case["name"]
@@ -285,3 +283,54 @@ def test_deterministic_across_runs_and_slice_lengths(cuda_lib):
         else:
             np.testing.assert_allclose(cur[2], first[2], atol=2e-6)
             np.testing.assert_allclose(cur[3][:, :2], first[3][:, :2], rtol=2e-6)
+
+
+FILTERED = [
+    # (workload index, V, B, top_k, top_p)
+    (0, None, None, 5, 1.0),      # fp32 rows of 1000, top-k only
+    (0, None, None, 20, 0.9),
+    (0, 50, 4, 0, 0.8),           # V <= 64: top-p over the whole vocabulary is served
+    (1, 20000, None, 20, 0.95),
+    (1, 20000, None, 64, 0.5),
+    (1, 20000, None, 1, 1.0),     # top-1: the argmax only
+    (2, 8191, 6, 64, 0.99),       # odd V: rows not 16-byte aligned
+    (3, 5003, 40, 20, 0.95),      # ragged lengths
+]
+
+
+@pytest.mark.parametrize("mode", [W.SAMPLE, W.GREEDY])
+@pytest.mark.parametrize("idx,V,B,top_k,top_p", FILTERED)
+def test_filtered_every_request(cuda_lib, idx, V, B, top_k, top_p, mode):
+    kw = {k: v for k, v in (("V", V), ("B", B)) if v is not None}
+    w = W.make_workload(W.WORKLOADS[idx], mode, seed=41 + idx, device=DEV, **kw)
+    run_and_compare(cuda_lib, w, top_k=top_k, top_p=top_p)
+
+
+def test_filtered_full_size_workload(cuda_lib):
+    """B=512 requests of block 16, V=262,144 bf16, top_k 20, top_p 0.95: every
+    request's outputs against the oracle on a sample of 16 requests."""
+    spec = W.WORKLOADS[4]
+    w = W.make_workload(spec, W.SAMPLE, seed=43, device=DEV)
+    reqs = sorted(np.random.default_rng(5).choice(w.B, 16, replace=False).tolist())
+    run_and_compare(cuda_lib, w, requests=reqs, want_stats=True)
+
+
+def test_filtered_ties_take_lowest_ids(cuda_lib):
+    """Rows full of equal logits: the kept set is the lowest ids."""
+    V, ell = 300, 3
+    t = torch.zeros((ell, V), dtype=torch.float32, device=DEV)
+    t[:, 7] = 2.0
+    d = torch.zeros((ell - 1, V), dtype=torch.float32, device=DEV)
+    w = _pair_workload(t, d, torch.tensor([7, 3], device=DEV), [ell],
+                       torch.tensor([0.5, 0.5, 0.3], device=DEV), mode=W.SAMPLE)
+    run_and_compare(cuda_lib, w, T=1.0, top_k=10, top_p=1.0)
+
+
+def test_filtered_top_k_above_limit_is_rejected(cuda_lib):
+    w = W.make_workload(W.WORKLOADS[1], W.SAMPLE, seed=44, device=DEV, V=2000)
+    with pytest.raises(cuda_lib.SpecVerifyError) as e:
+        cuda_lib.verify_workload(w, top_k=65, top_p=1.0)
+    assert e.value.status == -4
+    with pytest.raises(cuda_lib.SpecVerifyError) as e:
+        cuda_lib.verify_workload(w, top_k=0, top_p=0.9)  # top-p over 2000 tokens
+    assert e.value.status == -4
