@@ -87,15 +87,15 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t* a, int n) {
   __syncwarp();
 }
 
-// Keep the kmax largest keys of a warp's buffer (sorted, descending) and
-// return the new count; entries beyond it are cleared.
-__device__ __forceinline__ int warp_prune(uint64_t* cand, int cnt, int kmax) {
+// Keep the kmax largest of the first `cap` keys of a warp's buffer (sorted,
+// descending) and return the new count; entries beyond it are cleared.
+__device__ __forceinline__ int warp_prune(uint64_t* cand, int cnt, int kmax, int cap) {
   const int lane = threadIdx.x & 31;
   __syncwarp();
-  for (int i = cnt + lane; i < kCandCap; i += 32) cand[i] = 0;
-  warp_sort_desc(cand, kCandCap);
+  for (int i = cnt + lane; i < cap; i += 32) cand[i] = 0;
+  warp_sort_desc(cand, cap);
   const int keep = min(cnt, kmax);
-  for (int i = keep + lane; i < kCandCap; i += 32) cand[i] = 0;
+  for (int i = keep + lane; i < cap; i += 32) cand[i] = 0;
   __syncwarp();
   return keep;
 }
@@ -115,10 +115,16 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
   constexpr int UNROLL = 4;
   __shared__ uint64_t cand[kWarps][kCandCap];
   __shared__ uint64_t merged[kWarps * kMaxK];
+  __shared__ __align__(16) uint64_t bar_sh[kWarps];  // each warp's k-th best key
   __shared__ int bad_any;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
   const int K = P.top_k;
+  // buffer in use: the smallest power of two that holds k keys plus one
+  // vote's worth (32), so that the bar is raised often and stays close to
+  // the k-th best key seen so far
+  int cap = 64;
+  while (cap < K + 32) cap <<= 1;
   FiltRow* recs = reinterpret_cast<FiltRow*>(P.filt);
   const int32_t nrows = P.Nt + P.Nd;
 
@@ -132,13 +138,26 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
     uint64_t* my = cand[warp];
     for (int i = lane; i < kCandCap; i += 32) my[i] = 0;
     if (tid == 0) bad_any = 0;
+    if (tid < kWarps) bar_sh[tid] = 0ull;
     __syncthreads();
     int cnt = 0;        // warp-uniform
     uint64_t thr = 0;   // warp-uniform: only larger keys can still make the top k
+    float thr_val = -INFINITY;  // the logit of that key (the screen's bar)
     bool bad = false;
     // the loop runs on the warp's first vector, so that every lane takes
     // part in the warp-wide votes below; lanes past the end hold no element
     for (int32_t kw = warp * 32; kw < nv; kw += UNROLL * kThreads) {
+      // any warp's k-th best key bars the whole CTA: an element below it
+      // cannot be among the CTA's k best, so the highest of them is used
+      {
+        uint64_t b = thr;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) b = max(b, bar_sh[w]);
+        if (b > thr) {
+          thr = b;
+          thr_val = key_value(b);
+        }
+      }
       uint4 raw[UNROLL];
 #pragma unroll
       for (int q = 0; q < UNROLL; ++q) {
@@ -156,30 +175,65 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
           x[l] = ES == 2 ? ((l & 1) ? bf16hi(wv[l >> 1]) : bf16lo(wv[l >> 1]))
                          : __uint_as_float(wv[l]);
         const int32_t i0 = k * VEC - s.hoff;
+        // screen: a vector whose largest logit is below the warp's bar holds
+        // no candidate (a NaN maximum goes on to the exact path and is flagged)
+        float vm = x[0];
+#pragma unroll
+        for (int l = 1; l < VEC; ++l) vm = fmax_nan(vm, x[l]);
+        const bool maybe = k < nv && !(vm < thr_val);
+        if (!__any_sync(0xffffffffu, maybe)) continue;
+        // this lane's keys above the bar (NaN and +inf are flagged, not kept)
+        uint64_t key[VEC];
+        int c = 0;
 #pragma unroll
         for (int l = 0; l < VEC; ++l) {
           const int32_t id = i0 + l;
-          const bool valid = k < nv && id >= 0 && id < s.len;
+          const bool valid = maybe && id >= 0 && id < s.len;
           if (valid && (x[l] != x[l] || x[l] == INFINITY)) bad = true;
-          const uint64_t key =
-              valid && !(x[l] != x[l])
-                  ? (static_cast<uint64_t>(order_key(x[l])) << 32) | static_cast<uint32_t>(~id)
-                  : 0ull;
-          bool take = key > thr;
+          key[l] = valid && !(x[l] != x[l])
+                       ? (static_cast<uint64_t>(order_key(x[l])) << 32) | static_cast<uint32_t>(~id)
+                       : 0ull;
+          c += key[l] > thr;
+        }
+        int total = __reduce_add_sync(0xffffffffu, c);
+        if (total == 0) continue;
+        if (cnt + total <= cap) {  // one scan places every lane's keys
+          int pre = c;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, pre, o);
+            if (lane >= o) pre += y;
+          }
+          int at = cnt + pre - c;
+#pragma unroll
+          for (int l = 0; l < VEC; ++l)
+            if (key[l] > thr) my[at++] = key[l];
+          cnt += total;
+          continue;
+        }
+        // the buffer could overflow: element slot by element slot, pruning
+        // (keep the best K, raise the bar) whenever a slot would not fit
+#pragma unroll
+        for (int l = 0; l < VEC; ++l) {
+          bool take = key[l] > thr;
           unsigned m = __ballot_sync(0xffffffffu, take);
           if (!m) continue;
-          if (cnt + __popc(m) > kCandCap) {  // full: keep the best K, raise the bar
-            cnt = warp_prune(my, cnt, K);
-            thr = cnt >= K ? my[K - 1] : 0ull;
-            take = key > thr;
+          if (cnt + __popc(m) > cap) {
+            cnt = warp_prune(my, cnt, K, cap);
+            if (cnt >= K && my[K - 1] > thr) {
+              thr = my[K - 1];
+              thr_val = key_value(thr);
+              if (lane == 0) bar_sh[warp] = thr;
+            }
+            take = key[l] > thr;
             m = __ballot_sync(0xffffffffu, take);
           }
-          if (take) my[cnt + __popc(m & lt_mask)] = key;
+          if (take) my[cnt + __popc(m & lt_mask)] = key[l];
           cnt += __popc(m);
         }
       }
     }
-    cnt = warp_prune(my, cnt, K);
+    cnt = warp_prune(my, cnt, K, cap);
     for (int i = lane; i < kMaxK; i += 32) merged[warp * kMaxK + i] = i < K ? my[i] : 0ull;
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&bad_any, 1);
     __syncthreads();
