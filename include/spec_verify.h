@@ -37,10 +37,14 @@
  *
  * Ownership and memory.  The caller owns every buffer.  The library
  * allocates nothing: scratch lives in the caller's workspace (size from
- * spec_verify_workspace_size).  Device pointers must be device memory of
- * the current CUDA device.  The logits base pointers must be 16-byte
- * aligned; other device pointers 4-byte aligned; the workspace 256-byte
- * aligned.
+ * spec_verify_workspace_size), which must be zeroed once before its first
+ * use and can then be reused by any number of calls (the cross-CTA exchange
+ * tags every word with a per-call tag; zero is never a tag).  Device pointers
+ * must be device memory of the current CUDA device.  The logits base
+ * pointers must be 16-byte aligned; other device pointers 4-byte aligned;
+ * the workspace 256-byte aligned.  The kernels read the 16-byte blocks that
+ * cover each logits row, up to 15 bytes past the end of the last row when
+ * V * element size is not a multiple of 16.
  *
  * Streams.  Every call only enqueues work on `stream` (a cudaStream_t; NULL
  * is the legacy default stream) and returns without synchronising the host.
@@ -73,7 +77,7 @@ extern "C" {
 #define SV_ERR_ARG (-1)         /* null/misaligned pointer, bad size or parameter */
 #define SV_ERR_DTYPE (-2)       /* dtype is neither SV_BF16 nor SV_FP32 */
 #define SV_ERR_CUDA (-3)        /* a CUDA runtime call or a launch failed */
-#define SV_ERR_UNSUPPORTED (-4) /* filter combination or cluster shape not available */
+#define SV_ERR_UNSUPPORTED (-4) /* kept set above SV_MAX_FILTER_K tokens, or a shape not served */
 #define SV_ERR_WORKSPACE (-5)   /* workspace missing, misaligned or too small */
 #define SV_ERR_TOO_LARGE (-6)   /* spec_verify_static: more than SV_STATIC_MAX_ROWS rows */
 
@@ -114,10 +118,13 @@ size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows);
  *  temperature    T > 0 (required in sampling mode and whenever out_conf or
  *                 out_row_stats is requested; otherwise ignored).
  *  top_k          <= 0 or >= V: off.  Else keep the top_k tokens.
- *  top_p          in (0, 1]; 1 = off.  top_p < 1 needs 1 <= top_k <=
- *                 SV_MAX_FILTER_K (full-vocabulary top-p is not served:
- *                 SV_ERR_UNSUPPORTED); top_k in (SV_MAX_FILTER_K, V) is
- *                 likewise not served yet.
+ *  top_p          in (0, 1]; 1 = off.  With either filter on, the kept set
+ *                 (top_k if on, else V) must be at most SV_MAX_FILTER_K
+ *                 tokens, else SV_ERR_UNSUPPORTED (full-vocabulary top-p
+ *                 over V > 64 and top_k in (SV_MAX_FILTER_K, V) are not
+ *                 served).  Filtered calls run the top-k path: one pass per
+ *                 row selects the kept set exactly, then one warp per
+ *                 request decides on the kept sets.
  *  mode           SV_GREEDY or SV_SAMPLE.
  *  out_tokens     [N_t] int32 device: for request r, entries off_r .. off_r
  *                 + a_r - 1 = accepted drafts, entry off_r + a_r = the final
@@ -143,12 +150,15 @@ int spec_verify(const void* target_logits, const void* draft_logits,
                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * Phase 1 of spec_verify (same arguments; out_tokens and out_accept_len are
- * not touched).  One thread-block cluster per target row streams the target
- * row and its draft partner from HBM into the cluster's shared memory once,
- * and writes the per-row statistics, c* labels and per-position accept
- * decisions (into the workspace, and into out_conf / out_row_stats when
- * given).  This is the bandwidth-bound kernel.
+ * Phase 1 of spec_verify (same arguments; out_tokens, out_accept_len and
+ * out_conf are not touched).  Unfiltered: one persistent cooperative grid
+ * (one CTA per SM) streams every target row and its draft partner from HBM
+ * once, slice by slice through shared memory; the CTAs holding the slices of
+ * a row exchange partial statistics through the workspace, and the
+ * per-row statistics, accept decisions and per-slice label partials go to
+ * the workspace (row statistics also to out_row_stats when given).
+ * Filtered: one CTA per row selects the kept set into the workspace.  This
+ * is the bandwidth-bound phase.
  */
 int spec_verify_rows(const void* target_logits, const void* draft_logits,
                      const int32_t* draft_tokens, const float* uniforms,
@@ -161,7 +171,8 @@ int spec_verify_rows(const void* target_logits, const void* draft_logits,
 
 /*
  * Phase 2 of spec_verify (same arguments).  Per request: the first-rejection
- * scan over the accept decisions left in the workspace by phase 1, then the
+ * scan over the accept decisions left in the workspace by phase 1, the c*
+ * labels (sums of the per-slice partials, or over the kept sets), then the
  * final token -- in unfiltered sampling mode an inverse-CDF draw over the one
  * rejected row pair (or the bonus row) re-read from HBM -- and the outputs.
  * Must run after spec_verify_rows with identical arguments and workspace.

@@ -540,7 +540,8 @@ const char* spec_verify_status_string(int status) {
     case SV_ERR_ARG: return "invalid argument (null or misaligned pointer, bad size or parameter)";
     case SV_ERR_DTYPE: return "unknown logits dtype";
     case SV_ERR_CUDA: return "CUDA runtime or launch failure";
-    case SV_ERR_UNSUPPORTED: return "filter combination or cluster shape not supported";
+    case SV_ERR_UNSUPPORTED:
+      return "not served: kept set above SV_MAX_FILTER_K tokens, or a shape the kernels do not take";
     case SV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SV_ERR_TOO_LARGE:
       return "problem larger than the static scratch of spec_verify_static "
