@@ -276,20 +276,41 @@ __device__ __forceinline__ float2 sum_exp2_x2(const float* x, float2 sc2, float2
 // every lane of the warp using the same references (the warp maximum of the
 // lanes' first vectors), so the warp's partials are plain sums.  Returns
 // false, uniformly over the warp, on a non-finite input or an overflow (the
-// caller then runs the general path).
-template <int ES>
+// caller then runs the general path).  TRACKM: also the exact maximum of each
+// row and the lowest id holding it (v0 = vocabulary id of vector 0's first
+// element).
+template <int VEC>
+__device__ __forceinline__ void track_max(const float* x, float vm, int32_t id0, float& m,
+                                          int32_t& i) {
+  if (vm > m) {  // vectors are visited in increasing id order: the first maximum wins
+    int l0 = VEC - 1;
+#pragma unroll
+    for (int l = VEC - 2; l >= 0; --l)
+      if (x[l] == vm) l0 = l;
+    m = vm;
+    i = id0 + l0;
+  }
+}
+
+template <int ES, bool TRACKM>
 __device__ __forceinline__ bool pass1_pair_fast(const unsigned char* bt, const unsigned char* bd,
                                                 int32_t nv, float sc, int ct, int NT1, RStat& at,
-                                                RStat& ad) {
+                                                RStat& ad, int32_t v0) {
   constexpr int VEC = 16 / ES;
   float t[VEC], d[VEC];
   float mt = -INFINITY, md = -INFINITY;
+  float rmt = -INFINITY, rmd = -INFINITY;  // running maxima (TRACKM)
+  int32_t rit = 0x7fffffff, rid = 0x7fffffff;
   int32_t k = ct;
   if (k < nv) {
     load_vec_raw<ES>(bt, k, t);
     load_vec_raw<ES>(bd, k, d);
     mt = vmax_nan<VEC>(t);
     md = vmax_nan<VEC>(d);
+    if (TRACKM) {
+      track_max<VEC>(t, mt, v0 + k * VEC, rmt, rit);
+      track_max<VEC>(d, md, v0 + k * VEC, rmd, rid);
+    }
   }
   // NaN or +inf in a first vector: general path for the whole warp
   if (!__all_sync(0xffffffffu, !(mt != mt || md != md || mt == INFINITY || md == INFINITY)))
@@ -307,6 +328,10 @@ __device__ __forceinline__ bool pass1_pair_fast(const unsigned char* bt, const u
       load_vec_raw<ES>(bd, k, d);
       at2 = __fadd2_rn(at2, sum_exp2_x2<VEC>(t, sc2, nht));
       ad2 = __fadd2_rn(ad2, sum_exp2_x2<VEC>(d, sc2, nhd));
+      if (TRACKM) {
+        track_max<VEC>(t, vmax_nan<VEC>(t), v0 + k * VEC, rmt, rit);
+        track_max<VEC>(d, vmax_nan<VEC>(d), v0 + k * VEC, rmd, rid);
+      }
     }
   }
   float st = at2.x + at2.y, sd = ad2.x + ad2.y;
@@ -318,6 +343,12 @@ __device__ __forceinline__ bool pass1_pair_fast(const unsigned char* bt, const u
   }
   at = RStat{ht, st, -INFINITY, 0x7fffffff};
   ad = RStat{hd, sd, -INFINITY, 0x7fffffff};
+  if (TRACKM) {  // warp maximum, lowest id among the lanes holding it
+    at.m = warp_max_f32(rmt);
+    ad.m = warp_max_f32(rmd);
+    at.i = __reduce_min_sync(0xffffffffu, rmt == at.m ? rit : 0x7fffffff);
+    ad.i = __reduce_min_sync(0xffffffffu, rmd == ad.m ? rid : 0x7fffffff);
+  }
   return true;
 }
 
@@ -604,10 +635,10 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         bool bad = false;
         const Slice s_t = slice_t(info), s_d = slice_d(info);
         RStat a_t, a_d;
-        const bool fast = !TRACK && NEED_Z && info.pair && slice_aligned<ES>(s_t) &&
+        const bool fast = NEED_Z && info.pair && slice_aligned<ES>(s_t) &&
                           slice_aligned<ES>(s_d) &&
-                          pass1_pair_fast<ES>(sm.tbuf(s), sm.dbuf(s), s_t.nbytes >> 4, sc, ct, NT1,
-                                              a_t, a_d);
+                          pass1_pair_fast<ES, TRACK>(sm.tbuf(s), sm.dbuf(s), s_t.nbytes >> 4, sc,
+                                                     ct, NT1, a_t, a_d, s_t.v0);
         if (!fast) {  // general path: per-thread partials, then a warp merge
           a_t = pass1_thread<ES, NEED_Z, TRACK>(sm.tbuf(s), s_t, sc, ct, NT1, bad);
           a_d = info.pair ? pass1_thread<ES, NEED_Z, TRACK>(sm.dbuf(s), s_d, sc, ct, NT1, bad)
