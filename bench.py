@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--mode", choices=("sample", "greedy"), default="sample")
+    ap.add_argument("--requests", type=int, default=0,
+                    help="run the workload with this many requests instead of its own B "
+                         "(small cases for profiling; the timed default keeps B)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -256,7 +259,8 @@ def run_ours(args, world, rank, local):
     spec = W.WORKLOADS[args.workload]
     mode = W.SAMPLE if args.mode == "sample" else W.GREEDY
     seed = 1000 * args.workload + rank
-    sets = [W.make_workload(spec, mode, seed=seed + 100 * i, device=dev) for i in range(2)]
+    kw = {"B": args.requests} if args.requests > 0 else {}
+    sets = [W.make_workload(spec, mode, seed=seed + 100 * i, device=dev, **kw) for i in range(2)]
     w = sets[0]
     B, Nt, Nd, V = w.B, w.n_target_rows, w.n_draft_rows, w.V
     stream = torch.cuda.current_stream(dev)
@@ -317,7 +321,9 @@ def run_ours(args, world, rank, local):
     mean_rows_ms = statistics.fmean(rows_ms)
     achieved = bytes_per_launch / (mean_rows_ms / 1e3) / 1e9
     peak, peak_src = hbm_peak()
-    traffic = recorded_traffic(spec.name)
+    # the recorded traffic is for the full-size workload only
+    traffic = recorded_traffic(spec.name) if args.requests <= 0 else None
+    filtered = (0 < spec.top_k < V) or spec.top_p < 1.0
 
     e2e = None
     if not args.no_e2e:
@@ -344,7 +350,8 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "rows_kernel", "bytes_per_launch": bytes_per_launch,
+                         "kernel": "filter_rows_kernel" if filtered else "rows_kernel",
+                         "bytes_per_launch": bytes_per_launch,
                          "mean_launch_ms": mean_rows_ms, "peak_source": peak_src},
             "hbm_gbs_step": bytes_per_launch / (elapsed_ms / K / 1e3) / 1e9,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
