@@ -193,10 +193,18 @@ __device__ __forceinline__ float sum_exp2(const float* x, float sc, float h) {
   return e[0];
 }
 
+// Bound on a lane's sum in the passes whose reference is not the running
+// maximum (2^24): larger sums mean a reference far below the maximum (low
+// temperatures), where exponent arguments lose precision and the merge
+// factors 2^(h - H) of such partials can flush to zero while the product
+// does not; those lanes take the tracked variant instead.
+constexpr float kFastSumMax = 16777216.f;
+
 // Pass 1 of one consumer thread over its vectors k = ct, ct + NCT, ... of a
 // slice.  TRACK: exact running max / argmax.  Otherwise the reference h is
-// taken from the thread's first vector holding a finite value; an overflow or
-// a non-finite input sends the thread to the tracked variant (rare).
+// taken from the thread's first vector holding a finite value; a sum at or
+// above kFastSumMax or a non-finite input sends the thread to the tracked
+// variant (rare).
 template <int ES, bool NEED_Z, bool TRACK>
 __device__ __forceinline__ RStat pass1_thread(const unsigned char* buf, const Slice& s, float sc,
                                               int ct, int NCT, bool& bad) {
@@ -223,7 +231,7 @@ __device__ __forceinline__ RStat pass1_thread(const unsigned char* buf, const Sl
         load_vec<ES>(buf, s, k, x);
         st.s += sum_exp2<VEC>(x, sc, st.h);
       }
-      if (st.s < INFINITY) return st;  // finite: done
+      if (st.s < kFastSumMax) return st;  // in range: done
     } else if (k >= nv) {
       return st;  // nothing but -inf in this thread's vectors
     }
@@ -271,14 +279,7 @@ __device__ __forceinline__ float2 sum_exp2_x2(const float* x, float2 sc2, float2
   return acc;
 }
 
-// Pass 1 fast path of one warp of the pass-1 group for a slice pair with no
-// masked lanes, when the exact max is not needed: both rows in one loop,
-// every lane of the warp using the same references (the warp maximum of the
-// lanes' first vectors), so the warp's partials are plain sums.  Returns
-// false, uniformly over the warp, on a non-finite input or an overflow (the
-// caller then runs the general path).  TRACKM: also the exact maximum of each
-// row and the lowest id holding it (v0 = vocabulary id of vector 0's first
-// element).
+// Running maximum of one lane's vectors and the lowest id holding it.
 template <int VEC>
 __device__ __forceinline__ void track_max(const float* x, float vm, int32_t id0, float& m,
                                           int32_t& i) {
@@ -292,6 +293,14 @@ __device__ __forceinline__ void track_max(const float* x, float vm, int32_t id0,
   }
 }
 
+// Pass 1 fast path of one warp of the pass-1 group for a slice pair with no
+// masked lanes, when the exact max is not needed: both rows in one loop,
+// every lane of the warp using the same references (the warp maximum of the
+// lanes' first vectors), so the warp's partials are plain sums.  Returns
+// false, uniformly over the warp, on a non-finite input or a lane sum at or
+// above kFastSumMax (the caller then runs the general path).  TRACKM: also
+// the exact maximum of each row and the lowest id holding it (v0 =
+// vocabulary id of vector 0's first element).
 template <int ES, bool TRACKM>
 __device__ __forceinline__ bool pass1_pair_fast(const unsigned char* bt, const unsigned char* bd,
                                                 int32_t nv, float sc, int ct, int NT1, RStat& at,
@@ -335,7 +344,10 @@ __device__ __forceinline__ bool pass1_pair_fast(const unsigned char* bt, const u
     }
   }
   float st = at2.x + at2.y, sd = ad2.x + ad2.y;
-  if (!__all_sync(0xffffffffu, st < INFINITY && sd < INFINITY)) return false;
+  // every lane's sum below 2^24 keeps each exponent argument <= 24 (full
+  // fp32 precision of x sc - h) and the merged sums far from overflow, so a
+  // partial whose merge factor flushes to zero holds < 2^-90 of the row
+  if (!__all_sync(0xffffffffu, st < kFastSumMax && sd < kFastSumMax)) return false;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {  // two independent shuffle chains
     st += __shfl_xor_sync(0xffffffffu, st, off);

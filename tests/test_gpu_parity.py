@@ -334,3 +334,17 @@ def test_filtered_top_k_above_limit_is_rejected(cuda_lib):
     with pytest.raises(cuda_lib.SpecVerifyError) as e:
         cuda_lib.verify_workload(w, top_k=0, top_p=0.9)  # top-p over 2000 tokens
     assert e.value.status == -4
+
+
+@pytest.mark.parametrize("T", [0.02, 0.05, 0.1])
+@pytest.mark.parametrize("seed,V,B", [(60, 12000, 6), (61, 40000, 4), (62, 151936, 2), (63, 7001, 8)])
+@pytest.mark.parametrize("pass1", [8, 6, 10])
+def test_low_temperature_statistics(cuda_lib, T, seed, V, B, pass1):
+    """Low temperatures stretch the exponent range (sc = log2(e) / T), so the
+    first-vector references of the fast path are far from the row maxima and
+    overflow falls back to the exact path: statistics, labels and decisions
+    must still match the oracle, for several consumer-warp splits."""
+    w = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=seed, device=DEV, B=B, V=V)
+    with env(SPEC_VERIFY_PASS1_WARPS=pass1):
+        run_and_compare(cuda_lib, w, T=T)
+        run_and_compare(cuda_lib, w, T=T, mode=W.GREEDY)
