@@ -173,9 +173,13 @@ int spec_verify_rows(const void* target_logits, const void* draft_logits,
  * Phase 2 of spec_verify (same arguments).  Per request: the first-rejection
  * scan over the accept decisions left in the workspace by phase 1, the c*
  * labels (sums of the per-slice partials, or over the kept sets), then the
- * final token -- in unfiltered sampling mode an inverse-CDF draw over the one
- * rejected row pair (or the bonus row) re-read from HBM -- and the outputs.
- * Must run after spec_verify_rows with identical arguments and workspace.
+ * final token -- in unfiltered sampling mode an inverse-CDF draw that picks
+ * the vocabulary slice from the per-slice masses phase 1 left in the
+ * workspace and re-reads only that slice of the rejected row pair (or of the
+ * bonus row) from HBM -- and the outputs.  Must run after spec_verify_rows
+ * with identical arguments and workspace; kernels launched between the two
+ * on the stream must not write the workspace.  (spec_verify launches this
+ * phase so that it overlaps the end of phase 1.)
  */
 int spec_verify_finalize(const void* target_logits, const void* draft_logits,
                          const int32_t* draft_tokens, const float* uniforms,

@@ -60,8 +60,6 @@ int round_up(int v, int m) { return (v + m - 1) / m * m; }
 // Bytes of one row buffer for a slice of S elements (16-byte cover + slack).
 int rowbuf_bytes(int S, int es) { return round_up(S * es + 32, 128); }
 
-int slice_len(int V, int C, int es) { return round_up((V + C - 1) / C, 16 / es); }
-
 // Size k of the kept set under top-k / top-p filtering: 0 when unfiltered,
 // -1 when the set can exceed SV_MAX_FILTER_K tokens (not served).
 int filter_k(int V, int top_k, float top_p) {
@@ -100,34 +98,8 @@ int rows_geometry(int V, int B, int es, const DeviceCache& dc, RowsGeom* g) {
   return SV_ERR_UNSUPPORTED;  // rows too long for kMaxSlices slices in shared memory
 }
 
-// Cluster size of the unfiltered final draw (one request per cluster).
-int draw_cluster(int V, int es, const DeviceCache& dc, int* smem_out) {
-  const int forced = env_int("SPEC_VERIFY_DRAW_CLUSTER", 0);
-  for (int C = kMaxCluster; C >= 1; C /= 2) {
-    if (forced > 0 && C != forced) continue;
-    const int S = slice_len(V, C, es);
-    const int smem = kF_HdrBytes + 2 * rowbuf_bytes(S, es);
-    if (smem <= dc.max_smem_optin) {
-      *smem_out = smem;
-      return C;
-    }
-  }
-  return SV_ERR_UNSUPPORTED;
-}
-
-// The dynamic shared-memory limit is raised to the device maximum (not to
-// this launch's size), so that one setting serves every configuration.
-template <typename K>
-cudaError_t prepare_kernel(K kernel, int max_smem, int cluster) {
-  cudaError_t e =
-      cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem);
-  if (e == cudaSuccess && cluster > 8)
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  return e;
-}
-
-// Kernel attributes and the cluster-occupancy check are host calls that can
-// cost microseconds; they run once per (device, kernel, smem, cluster size).
+// Kernel attributes and the occupancy check are host calls that can cost
+// microseconds; they run once per (device, kernel, smem, cluster size).
 struct PreparedKey {
   int dev;
   const void* fn;
@@ -153,42 +125,48 @@ void remember_prepared(int dev, const void* fn, int smem, int C, int status) {
   if (g_nprepared < kMaxPrepared) g_prepared[g_nprepared++] = PreparedKey{dev, fn, smem, C, status};
 }
 
-// Launch `kernel` with clusters of C CTAs of `threads` threads.  nclusters
-// > 0: that many clusters; nclusters < 0: one persistent wave of
-// min(-nclusters, resident clusters) clusters.
+// Launch `grid` CTAs of `threads` threads with `smem` bytes of dynamic
+// shared memory.  Above the default 48 KB the kernel's dynamic limit is
+// raised to the device maximum (not to this launch's size) once, so that one
+// setting serves every configuration.  `dependent`: launch as a programmatic
+// dependent of the previous kernel on the stream, which then must be this
+// library's rows kernel of the same call (the kernel reads only the call's
+// inputs before grid_dep_wait, and the rows kernel writes none of them).
 template <typename K>
-int launch_cluster(K kernel, const Params& P, int nclusters, int C, int threads, int smem,
-                   int max_smem, cudaStream_t stream) {
+int launch_plain(K kernel, const Params& P, int grid, int threads, int smem, int max_smem,
+                 bool dependent, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
   const void* fn = reinterpret_cast<const void*>(kernel);
-  int status = find_prepared(dev, fn, smem, C);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, 1, 1);
-  cfg.blockDim = dim3(threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  int status = find_prepared(dev, fn, smem, 1);
   if (status == -1000) {
-    int active = 0;
-    if (prepare_kernel(kernel, max_smem, C) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&active, kernel, &cfg) != cudaSuccess)
+    int n = 0;
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
+    // kernels that may need more than the default 48 KB: the limit goes to
+    // the device maximum less the kernel's static shared memory
+    if (e == cudaSuccess && smem > 48 * 1024)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               max_smem - static_cast<int>(fa.sharedSizeBytes));
+    if (e != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess)
       status = SV_ERR_CUDA;
     else
-      status = active > 0 ? active : SV_ERR_UNSUPPORTED;
-    remember_prepared(dev, fn, smem, C, status);
+      status = n > 0 ? n : SV_ERR_UNSUPPORTED;
+    remember_prepared(dev, fn, smem, 1, status);
   }
   if (status <= 0) return status == 0 ? SV_ERR_UNSUPPORTED : status;
-  const int n = nclusters > 0 ? nclusters : std::min(-nclusters, status);  // status = resident
-  cfg.gridDim = dim3(static_cast<unsigned>(n) * C, 1, 1);
-  if (cudaLaunchKernelEx(&cfg, kernel, P) != cudaSuccess) return SV_ERR_CUDA;
-  return SV_OK;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = dependent ? attr : nullptr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, P) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -393,35 +371,35 @@ int run_rows(const Args& a) {
                    : launch_rows<4, 16>(P, smem, dc, need_z, need_conf, track, st);
 }
 
-int run_finalize(const Args& a) {
+// `after_rows`: the rows kernel of this same call was the last launch on the
+// stream (the finalize kernel then overlaps its start with that kernel's end).
+int run_finalize(const Args& a, bool after_rows) {
   DeviceCache dc;
   int rc = device_info(&dc);
   if (rc != SV_OK) return rc;
   Params P = make_params(a);
   const int es = a.dtype == SV_BF16 ? 2 : 4;
   cudaStream_t st = static_cast<cudaStream_t>(a.stream);
-  if (P.top_k > 0) {  // top-k / top-p: decisions on the kept sets, one warp per request
-    filter_requests_kernel<<<(a.B + kWarps - 1) / kWarps, kThreads, 0, st>>>(P);
-    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
-  }
+  const int per_warp_grid = (a.B + kWarps - 1) / kWarps;
+  if (P.top_k > 0)  // top-k / top-p: decisions on the kept sets, one warp per request
+    return launch_plain(filter_requests_kernel, P, per_warp_grid, kThreads, 0, dc.max_smem_optin,
+                        after_rows, st);
   RowsGeom geo;
   rc = rows_geometry(a.V, a.B, es, dc, &geo);
   if (rc != SV_OK) return rc;
   P.nslices = geo.S;
-  if (a.mode == SV_GREEDY) {
-    finalize_select_kernel<<<(a.B + kWarps - 1) / kWarps, kThreads, 0, st>>>(P);
-    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
-  }
-  int smem = 0;
-  const int C4 = draw_cluster(a.V, es, dc, &smem);
-  if (C4 < 0) return C4;
-  P.S4 = slice_len(a.V, C4, es);
-  P.rowbuf4 = rowbuf_bytes(P.S4, es);
+  if (a.mode == SV_GREEDY)
+    return launch_plain(finalize_select_kernel, P, per_warp_grid, kThreads, 0, dc.max_smem_optin,
+                        after_rows, st);
+  // unfiltered sampling: one CTA per request re-reads one slice pair
+  P.S = geo.L;
+  P.rowbuf = rowbuf_bytes(geo.L, es);
+  const int smem = kD_HdrBytes + 2 * P.rowbuf;
   if (es == 2)
-    return launch_cluster(finalize_draw_kernel<2>, P, a.B, C4, kThreads, smem, dc.max_smem_optin,
-                          st);
-  return launch_cluster(finalize_draw_kernel<4>, P, a.B, C4, kThreads, smem, dc.max_smem_optin,
-                        st);
+    return launch_plain(finalize_draw_kernel<2>, P, a.B, kDrawThreads, smem, dc.max_smem_optin,
+                        after_rows, st);
+  return launch_plain(finalize_draw_kernel<4>, P, a.B, kDrawThreads, smem, dc.max_smem_optin,
+                      after_rows, st);
 }
 
 // ---------------------------------------------------------------- static scratch
@@ -501,14 +479,14 @@ int spec_verify_rows(SV_ARGS_DECL) {
 int spec_verify_finalize(SV_ARGS_DECL) {
   SV_ARGS_PACK;
   const int rc = sv::check_args(a);
-  return rc != SV_OK ? rc : sv::run_finalize(a);
+  return rc != SV_OK ? rc : sv::run_finalize(a, false);
 }
 
 int spec_verify(SV_ARGS_DECL) {
   SV_ARGS_PACK;
   int rc = sv::check_args(a);
   if (rc == SV_OK) rc = sv::run_rows(a);
-  if (rc == SV_OK) rc = sv::run_finalize(a);
+  if (rc == SV_OK) rc = sv::run_finalize(a, true);
   return rc;
 }
 
@@ -530,7 +508,7 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
   SV_ARGS_PACK;
   rc = sv::check_args(a);
   if (rc == SV_OK) rc = sv::run_rows(a);
-  if (rc == SV_OK) rc = sv::run_finalize(a);
+  if (rc == SV_OK) rc = sv::run_finalize(a, true);
   return rc;
 }
 

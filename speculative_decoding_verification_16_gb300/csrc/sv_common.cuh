@@ -28,6 +28,19 @@ struct RowRec {
 };
 static_assert(sizeof(RowRec) == 32, "RowRec layout");
 
+// Published pass-1 partials of the rows kernel, kept in the workspace for
+// the rest of the call: per (target row g, slice k) kPartWords 64-bit words
+// at parts + (g * kMaxSlices + k) * kPartWords; word w carries the call's
+// tag in its upper and value w of the enum below in its lower 32 bits.
+// Slice k covers vocabulary ids [k * L, min(V, (k + 1) * L)) for the slice
+// length L of the call.  (h, s) pairs are partial statistics sum 2^(x sc) =
+// s * 2^h over the slice; m / i the slice maximum and the lowest id holding
+// it (greedy or statistics only); x the logits at the drafted token when the
+// slice holds it.
+constexpr int kMaxSlices = 32;  // slices per row
+constexpr int kPartWords = 16;  // 64-bit words per published partial (12 used)
+enum { R_HT = 0, R_ST, R_MT, R_IT, R_HD, R_SD, R_MD, R_ID, R_BAD, R_XT, R_XD, R_HASX, R_NWORDS };
+
 struct Params {
   const unsigned char* tgt;
   const unsigned char* drf;
@@ -47,16 +60,14 @@ struct Params {
   float* out_row_stats;
   int32_t* dev_error;
   RowRec* rec;
-  float* cpart;      // [N_t][32] label partial of each (row, slice) unit
+  float* cpart;      // [N_t][kMaxSlices] label partial of each (row, slice): sum of min(p_t, p_d)
   void* parts;       // [N_t][32][16] words: published pass-1 partials
   void* filt;        // filtered path: FiltRow per target row, then per draft row
   uint32_t tag;      // per-call tag of the published partials (never 0)
   int32_t nslices;   // slices per row of the rows kernel (<= 32)
   int32_t nunits;    // N_t * nslices
-  int32_t S;         // slice length (elements) of the rows kernel
-  int32_t S4;        // vocabulary slice per CTA of the finalize kernel
-  int32_t rowbuf;    // bytes of one row buffer in shared memory (rows kernel)
-  int32_t rowbuf4;   // bytes of one row buffer in shared memory (finalize kernel)
+  int32_t S;         // slice length L (elements) of the rows kernel
+  int32_t rowbuf;    // bytes of one slice buffer in shared memory
   int32_t nstages;   // shared-memory stages of the rows kernel
   int32_t offs_smem; // row_offsets copied into shared memory (B + 1 <= kMaxSmemOffsets)
   int32_t nw1;       // rows kernel, labels on: consumer warps running pass 1

@@ -127,6 +127,7 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
   while (cap < K + 32) cap <<= 1;
   FiltRow* recs = reinterpret_cast<FiltRow*>(P.filt);
   const int32_t nrows = P.Nt + P.Nd;
+  grid_dep_launch_dependents();
 
   for (int32_t row = blockIdx.x; row < nrows; row += gridDim.x) {
     const bool is_t = row < P.Nt;
@@ -351,6 +352,7 @@ __global__ void __launch_bounds__(kThreads) filter_requests_kernel(const Params 
     if (lane == 0) raise_error(P, SV_DEVERR_LEN);
     return;
   }
+  grid_dep_wait();  // the row records come from filter_rows_kernel
   int flags = 0;
   // labels of every drafted position, and the accept chain up to the first failure
   int32_t a = ell - 1;

@@ -9,27 +9,30 @@
 //                       request's last uniform from max(0, p_t - p_d) of the
 //                       rejected row pair, or from p_t of the bonus row after
 //                       a fully accepted block (DFlash / Spec V2 page, A3 and
-//                       its Leviathan et al. citation).  Only that one row
-//                       pair is read again from HBM.
+//                       its Leviathan et al. citation).
 //
-// The unfiltered draw runs on a cluster of C4 CTAs per request: CTA `rank`
-// owns a contiguous vocabulary slice, each thread a contiguous run of it, so
-// that running sums in (CTA rank, thread, element) order are sums in
-// ascending token id.  Partial masses are exchanged through distributed
-// shared memory and the one thread whose run holds the target mass walks it.
+// The unfiltered draw runs on one CTA per request in two steps.  The slice
+// is chosen first from per-slice masses the rows kernel left in the
+// workspace: the target mass P_k of slice k from its pass-1 partial, and for
+// a residual draw R_k = max(0, P_k - C_k) with C_k = sum of min(p_t, p_d)
+// over the slice (the slice's label partial).  Only the chosen slice pair is
+// then read again from HBM and walked element by element with the mass left
+// over: running sums in (thread, element) order are sums in ascending token
+// id.  fp32 slice masses differ from the exact ones by a few 1e-7 in
+// probability, inside the near-tie margin the oracle reports.
 #pragma once
 
 #include "sv_common.cuh"
 
 namespace sv {
 
-constexpr int kF_OffBars = 0;
-constexpr int kF_OffMass = 64;                                  // 2 rounds x kMaxCluster floats
-constexpr int kF_OffScan = kF_OffMass + 2 * kMaxCluster * 4;    // kThreads floats
-constexpr int kF_OffWarp = kF_OffScan + kThreads * 4;           // kWarps words
-constexpr int kF_OffInfo = kF_OffWarp + 32 * 4;                 // request info
-constexpr int kF_HdrBytes = 2048;
-static_assert(kF_OffInfo + 64 <= kF_HdrBytes, "finalize header");
+constexpr int kDrawThreads = 512;  // threads per CTA of the draw kernel
+constexpr int kDrawWarps = kDrawThreads / 32;
+constexpr int kD_OffBar = 0;    // mbarrier of the slice copies
+constexpr int kD_OffSel = 64;   // DrawSel
+constexpr int kD_OffRed = 128;  // [kDrawWarps] reduction scratch (floats / ints)
+constexpr int kD_HdrBytes = 1024;
+static_assert(kD_OffRed + 4 * kDrawWarps <= kD_HdrBytes, "draw header");
 
 struct ReqInfo {
   int32_t ok, off, ell, a, residual, pad[3];
@@ -103,187 +106,235 @@ __device__ __forceinline__ float warp_incl_scan(float v) {
   return v;
 }
 
-// Block-wide min / max of an int; every thread gets the result.
+// Block-wide min of an int over NW warps; every thread gets the result.
+template <int NW>
 __device__ __forceinline__ int block_min_int(int v, int* scratch) {
   v = __reduce_min_sync(0xffffffffu, v);
   if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
   __syncthreads();
   int r = scratch[0];
-  for (int w = 1; w < kWarps; ++w) r = min(r, scratch[w]);
+  for (int w = 1; w < NW; ++w) r = min(r, scratch[w]);
   __syncthreads();
   return r;
 }
 
-__device__ __forceinline__ int block_max_int(int v, int* scratch) {
-  v = __reduce_max_sync(0xffffffffu, v);
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+// Prefix bounds over the block of one float v >= 0 per thread, in thread
+// order: thread t's interval [lo, hi) of the running sum, built so that hi
+// of one thread and lo of the next are the same float (the intervals tile
+// [0, total) with no gap or overlap whatever the rounding), and the total
+// (equal to hi of the last thread).  Every thread gets its own bounds.
+template <int NW>
+__device__ __forceinline__ void block_scan_bounds(float v, float* scratch, float& lo, float& hi,
+                                                  float& total) {
+  const int lane = threadIdx.x & 31, w0 = threadIdx.x >> 5;
+  const float incl = warp_incl_scan(v);
+  const float prev = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 31) scratch[w0] = incl;
   __syncthreads();
-  int r = scratch[0];
-  for (int w = 1; w < kWarps; ++w) r = max(r, scratch[w]);
-  __syncthreads();
-  return r;
-}
-
-template <int ES>
-__global__ void __launch_bounds__(kThreads) finalize_draw_kernel(const Params P) {
-  extern __shared__ __align__(128) unsigned char smem[];
-  const uint32_t rank = cluster_ctarank();
-  const uint32_t csize = cluster_nctarank();
-  const int32_t r = static_cast<int32_t>(cluster_id_x());
-  const int tid = threadIdx.x;
-  float* scan = reinterpret_cast<float*>(smem + kF_OffScan);
-  int* wscr = reinterpret_cast<int*>(smem + kF_OffWarp);
-  ReqInfo* sinfo = reinterpret_cast<ReqInfo*>(smem + kF_OffInfo);
-  unsigned char* buf_t = smem + kF_HdrBytes;
-  unsigned char* buf_d = buf_t + P.rowbuf4;
-  const uint32_t bar = smem_addr(smem + kF_OffBars);
-
-  cluster_arrive_relaxed();
-  if (tid < 32) {
-    const ReqInfo rq = scan_request(P, r, tid);
-    if (tid == 0) {
-      *sinfo = rq;
-      mbar_init(bar, 1);
-      fence_mbar_init();
-    }
+  float base = 0.f, tot = 0.f;
+  for (int w = 0; w < NW; ++w) {
+    if (w < w0) base += scratch[w];
+    tot += scratch[w];
   }
   __syncthreads();
-  const ReqInfo q = *sinfo;
-  if (!q.ok) {  // uniform across the cluster: every CTA read the same request
-    if (rank == 0 && tid == 0) raise_error(P, SV_DEVERR_LEN);
-    cluster_wait_acquire();
+  lo = lane == 0 ? base : base + prev;
+  hi = base + incl;
+  total = tot;
+}
+
+// The slice chosen for a draw: slice index (-1: no mass anywhere), the mass
+// to pass inside it (probability units), the kind of draw and the stopping
+// row's record.
+struct DrawSel {
+  int32_t k;
+  int32_t residual;
+  float need;
+  int32_t pad;
+  RowRec rec;  // record of the stopping row
+};
+static_assert(kD_OffSel + sizeof(DrawSel) <= kD_OffRed, "draw header");
+
+__device__ __forceinline__ uint64_t ld_cg_u64(const uint64_t* p) {
+  uint64_t v;
+  asm volatile("ld.global.cg.b64 %0, [%1];" : "=l"(v) : "l"(p));
+  return v;
+}
+
+// Unfiltered sampling: one CTA per request.  For requests of at most
+// kDrawWarps rows warp j reads target row off + j as if it were the stopping
+// row (its record and slice masses, one lane per slice) while thread j reads
+// row j's accept flag, so the masses of the stopping row are in registers as
+// soon as a_r is known (longer requests: warp 0 reads them afterwards); that
+// warp picks the slice and the block walks it.  A slice whose recomputed
+// weights turn out all zero (its fp32 mass was rounding only) is dropped and
+// the choice repeated.
+template <int ES>
+__global__ void __launch_bounds__(kDrawThreads) finalize_draw_kernel(const Params P) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int32_t r = static_cast<int32_t>(blockIdx.x);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  DrawSel* sel = reinterpret_cast<DrawSel*>(smem + kD_OffSel);
+  float* fred = reinterpret_cast<float*>(smem + kD_OffRed);
+  int* ired = reinterpret_cast<int*>(smem + kD_OffRed);
+  unsigned char* buf_t = smem + kD_HdrBytes;
+  unsigned char* buf_d = buf_t + P.rowbuf;
+  const uint32_t bar = smem_addr(smem + kD_OffBar);
+  const uint64_t* parts = reinterpret_cast<const uint64_t*>(P.parts);
+
+  // ---- inputs only, before the rows kernel has finished
+  const int32_t off = __ldg(P.offs + r), off1 = __ldg(P.offs + r + 1), ell = __ldg(P.lens + r);
+  const bool ok = ell >= 1 && ell <= P.max_len && off1 - off == ell && off >= r &&
+                  off1 <= P.Nt && (r != 0 || off == 0) && (r != P.B - 1 || off1 == P.Nt) &&
+                  off - r + ell - 1 <= P.Nd;
+  if (!ok) {  // uniform over the CTA
+    if (tid == 0) raise_error(P, SV_DEVERR_LEN);
     return;
   }
-  const int32_t trow_i = q.off + q.a;
-  const int32_t drow_i = q.off - r + q.a;
-  const RowRec rr = P.rec[trow_i];
-  const unsigned char* trow = P.tgt + static_cast<size_t>(trow_i) * P.V * ES;
-  const unsigned char* drow = P.drf + static_cast<size_t>(drow_i) * P.V * ES;
-  const Slice s_t = make_slice<ES>(trow, P.V, rank, P.S4);
-  Slice s_d = make_slice<ES>(drow, P.V, rank, P.S4);
-  if (!q.residual) s_d.nbytes = 0, s_d.len = 0;
+  const float u = __ldg(P.uniforms + off + ell - 1);
+  const int32_t xtok = tid < ell - 1 ? __ldg(P.draft_tokens + off - r + tid) : -1;
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar, static_cast<uint32_t>(s_t.nbytes + s_d.nbytes));
-    if (s_t.nbytes) bulk_g2s(smem_addr(buf_t), s_t.gsrc, s_t.nbytes, bar);
-    if (s_d.nbytes) bulk_g2s(smem_addr(buf_d), s_d.gsrc, s_d.nbytes, bar);
+    mbar_init(bar, 1);
+    fence_mbar_init();
   }
+  grid_dep_wait();  // row records, label partials and pass-1 partials from the rows kernel
+
+  // slice masses of target row off + j as the stopping row, one lane per
+  // slice: P_k, and for a drafted row the residual mass R_k (w)
+  bool resid = false;
+  float w = 0.f, pk = 0.f;
+  RowRec rj{};
+  auto load_masses = [&](int32_t j) {
+    const int32_t g = off + j;
+    resid = j < ell - 1;
+    rj = P.rec[g];
+    if (lane < P.nslices) {
+      const uint64_t* pw = parts + (static_cast<size_t>(g) * kMaxSlices + lane) * kPartWords;
+      const float h = __uint_as_float(static_cast<uint32_t>(ld_cg_u64(pw + R_HT)));
+      const float s = __uint_as_float(static_cast<uint32_t>(ld_cg_u64(pw + R_ST)));
+      pk = h > -INFINITY ? s * exp2f(h - rj.mt) / rj.zt : 0.f;
+      w = pk;
+      if (resid)
+        w = fmaxf(0.f, pk - __ldcg(P.cpart + static_cast<size_t>(g) * kMaxSlices + lane));
+    }
+  };
+  const bool spec = ell <= kDrawWarps;
+  if (spec && warp < ell) load_masses(warp);
+  if (warp == 1) sum_labels(P, r, off, ell, lane);
+  // thread j: accept flag and error flags of row j (threads cover l_r <= SV_MAX_LEN)
+  int32_t first = ell - 1, rflags = 0;
+  if (tid < ell) {
+    rflags = __ldcg(&P.rec[off + tid].flags);
+    if (tid < ell - 1 && !__ldcg(&P.rec[off + tid].acc)) first = tid;
+  }
+  const int32_t a = block_min_int<kDrawWarps>(first, ired);  // first rejected position
+  const int sw = spec ? a : 0;  // the warp that holds the stopping row's masses
+  if (!spec && warp == 0) load_masses(a);
+  const int32_t trow_i = off + a;
+  // accepted drafts, -1 after the final token, flags of the rows up to a_r
+  if (tid < ell) {
+    if (tid < a) P.out_tokens[off + tid] = xtok;
+    else if (tid > a) P.out_tokens[off + tid] = -1;
+    if (tid <= a && rflags) raise_error(P, rflags);
+  }
+
   bool timeout = false;
-  mbar_wait(bar, 0, timeout);
-  const bool any_timeout = __syncthreads_or(timeout ? 1 : 0) != 0;
-
-  const float sc = P.sc;
-  DrawRow dr;
-  dr.sc = sc;
-  dr.ht = rr.mt;
-  dr.hd = rr.md;
-  dr.ratio = rr.zt / rr.zd;
-  dr.residual = q.residual;
-  if (rank == 0 && (tid >> 5) == 1) sum_labels(P, r, q.off, q.ell, tid & 31);
-  const int32_t E = (s_t.len + kThreads - 1) / kThreads;  // elements per thread
-  const int32_t i0 = min(s_t.len, tid * E), i1 = min(s_t.len, i0 + E);
-  const float u = __ldg(P.uniforms + q.off + q.ell - 1);
-
-  cluster_wait_acquire();  // all CTAs started: DSMEM stores allowed from here
-  // Two rounds at most: if the residual mass is zero the draw falls back to p_t.
-  for (int round = 0; round < 2; ++round) {
-    float* mass = reinterpret_cast<float*>(smem + kF_OffMass) + round * kMaxCluster;
-    // this thread's run, summed in ascending id order
-    float wsum = 0.f;
-    for (int32_t i = i0; i < i1; ++i) {
-      const float t = slice_elem<ES>(buf_t, s_t, i);
-      const float d = dr.residual ? slice_elem<ES>(buf_d, s_d, i) : 0.f;
-      wsum += dr.w(t, d);
-    }
-    // exclusive prefix of the per-thread sums inside the CTA (fixed order)
-    const float incl = warp_incl_scan(wsum);
-    float* wtot = reinterpret_cast<float*>(wscr);
-    if ((tid & 31) == 31) wtot[tid >> 5] = incl;
-    __syncthreads();
-    float wbase = 0.f, cta_total = 0.f;
-    for (int w = 0; w < kWarps; ++w) {
-      if (w < (tid >> 5)) wbase += wtot[w];
-      cta_total += wtot[w];
-    }
-    const float excl = wbase + (incl - wsum);
-    scan[tid] = excl;
-    __syncthreads();
-    // CTA totals to every CTA of the cluster
-    if (tid < static_cast<int>(csize))
-      st_cluster_u32(mapa(smem_addr(mass + rank), tid), __float_as_uint(cta_total));
-    cluster_arrive_release();
-    cluster_wait_acquire();
-    float total = 0.f, prefix = 0.f;
-    for (uint32_t c = 0; c < csize; ++c) {
-      if (c < rank) prefix += mass[c];
-      total += mass[c];
-    }
-    if (round == 0 && dr.residual && !(total > 0.f)) {  // no residual mass: draw from p_t
-      dr.residual = false;
-      continue;
-    }
-    const float target = u * total;
-    // owning CTA: first with positive mass whose range passes the target,
-    // else the last with positive mass
-    int owner = -1, last_pos = -1;
-    float pc = 0.f;
-    for (uint32_t c = 0; c < csize; ++c) {
-      if (mass[c] > 0.f) {
-        last_pos = static_cast<int>(c);
-        if (owner < 0 && target < pc + mass[c]) owner = static_cast<int>(c);
+  bool picked = false;
+  uint32_t phase = 0;  // parity of the copy barrier's current phase
+  for (int attempt = 0; attempt <= P.nslices; ++attempt, phase ^= 1u) {
+    if (warp == sw) {  // choose the slice: first whose interval passes u * total
+      float incl = warp_incl_scan(w);
+      float total = __shfl_sync(0xffffffffu, incl, 31);
+      if (resid && !(total > 0.f)) {  // no residual mass (rounding only): draw from p_t
+        resid = false;
+        w = pk;
+        incl = warp_incl_scan(w);
+        total = __shfl_sync(0xffffffffu, incl, 31);
       }
-      pc += mass[c];
-    }
-    if (owner < 0) owner = last_pos;
-    if (owner < 0) {  // no mass anywhere: non-finite statistics
-      if (rank == 0 && tid == 0) {
-        raise_error(P, SV_DEVERR_NAN);
-        P.out_tokens[trow_i] = rr.argt;
+      const float target = u * total;
+      const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && target < incl);
+      const unsigned pos = __ballot_sync(0xffffffffu, w > 0.f);
+      const int k = hit ? __ffs(hit) - 1 : (pos ? 31 - __clz(pos) : -1);
+      if (lane == 0) {
+        sel->k = k;
+        sel->residual = resid;
+        sel->rec = rj;
       }
+      if (lane == k) sel->need = fmaxf(0.f, target - (incl - w));
+    }
+    __syncthreads();
+    const int32_t k = sel->k;
+    const bool residual = sel->residual != 0;
+    if (k < 0) break;  // no mass anywhere: non-finite statistics
+    const Slice s_t = make_slice<ES>(P.tgt + static_cast<size_t>(trow_i) * P.V * ES, P.V, k, P.S);
+    Slice s_d = make_slice<ES>(P.drf + static_cast<size_t>(off - r + a) * P.V * ES, P.V, k, P.S);
+    if (!residual) s_d.nbytes = 0, s_d.len = 0;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(bar, static_cast<uint32_t>(s_t.nbytes + s_d.nbytes));
+      if (s_t.nbytes) bulk_g2s(smem_addr(buf_t), s_t.gsrc, s_t.nbytes, bar);
+      if (s_d.nbytes) bulk_g2s(smem_addr(buf_d), s_d.gsrc, s_d.nbytes, bar);
+    }
+    mbar_wait(bar, phase, timeout);
+    if (__syncthreads_or(timeout ? 1 : 0)) {
+      timeout = true;
       break;
     }
-    if (static_cast<int>(rank) == owner) {
-      const float local = target - prefix;  // target mass inside this CTA
-      const bool pos = wsum > 0.f;
-      const bool hit = pos && local < excl + wsum;
-      int own = block_min_int(hit ? tid : kThreads, wscr);
-      const int lastp = block_max_int(pos ? tid : -1, wscr);
-      if (own == kThreads) own = lastp;
-      if (tid == own) {
-        const float need = local - excl;  // mass to pass inside this run
+    const RowRec rr = sel->rec;
+    DrawRow dr;
+    dr.sc = P.sc;
+    dr.ht = rr.mt;
+    dr.hd = rr.md;
+    dr.ratio = rr.zt / rr.zd;
+    dr.residual = residual;
+    // weights in units of 1 / z_t: the mass to pass is need * z_t
+    const float need = sel->need * rr.zt;
+    const int32_t E = (s_t.len + kDrawThreads - 1) / kDrawThreads;  // elements per thread
+    const int32_t i0 = min(s_t.len, tid * E), i1 = min(s_t.len, i0 + E);
+    float wsum = 0.f;
+#pragma unroll 4
+    for (int32_t i = i0; i < i1; ++i) {
+      const float t = slice_elem<ES>(buf_t, s_t, i);
+      const float d = residual ? slice_elem<ES>(buf_d, s_d, i) : 0.f;
+      wsum += dr.w(t, d);
+    }
+    float lo, hi, tot;
+    block_scan_bounds<kDrawWarps>(wsum, fred, lo, hi, tot);
+    if (tot > 0.f) {
+      // the owner: the run whose interval holds `need`, or the last run with
+      // positive weight when rounding left need >= tot
+      const bool own = lo < hi && ((lo <= need && need < hi) || (need >= tot && hi == tot));
+      if (own) {
+        const float left = need - lo;  // mass to pass inside this run
         float run = 0.f;
-        int32_t pick = -1, last = -1;
+        int32_t p = -1, last = -1;
         for (int32_t i = i0; i < i1; ++i) {
           const float t = slice_elem<ES>(buf_t, s_t, i);
-          const float d = dr.residual ? slice_elem<ES>(buf_d, s_d, i) : 0.f;
+          const float d = residual ? slice_elem<ES>(buf_d, s_d, i) : 0.f;
           const float wv = dr.w(t, d);
           run += wv;
           if (wv > 0.f) last = i;
-          if (run > need) {
-            pick = i;
+          if (run > left) {
+            p = i;
             break;
           }
         }
-        if (pick < 0) pick = last;
-        P.out_tokens[trow_i] = s_t.v0 + pick;
+        if (p < 0) p = last;
+        P.out_tokens[trow_i] = s_t.v0 + p;
       }
+      picked = true;
+      break;
     }
-    break;
+    // every weight of the slice is zero: drop it and choose again
+    if (warp == sw && lane == k) w = 0.f;
+    __syncthreads();  // the buffers are free again before the next copy
   }
-
-  if (rank == 0 && tid < 32) {  // accepted drafts, -1 after the final token, flags
-    if (tid == 0) P.out_accept_len[r] = q.a;
-    int flags = 0;
-    for (int32_t j = tid; j < q.ell; j += 32) {
-      if (j < q.a) P.out_tokens[q.off + j] = __ldg(P.draft_tokens + q.off - r + j);
-      else if (j > q.a) P.out_tokens[q.off + j] = -1;
-      if (j <= q.a) flags |= P.rec[q.off + j].flags;
-    }
-    flags = __reduce_or_sync(0xffffffffu, flags) | (any_timeout ? SV_DEVERR_TIMEOUT : 0);
-    if (tid == 0 && flags) raise_error(P, flags);
+  if (!picked && tid == 0) {  // no mass anywhere (or a wait gave up)
+    raise_error(P, timeout ? SV_DEVERR_TIMEOUT : SV_DEVERR_NAN);
+    P.out_tokens[trow_i] = P.rec[trow_i].argt;
   }
-  if (any_timeout) {  // one more bounded wait for a copy still in flight
+  if (warp == 0 && lane == 0) P.out_accept_len[r] = a;
+  if (timeout) {  // one more bounded wait for a copy still in flight
     bool again = false;
-    mbar_wait(bar, 0, again);
+    mbar_wait(bar, phase, again);
   }
 }
 
@@ -293,6 +344,7 @@ __global__ void __launch_bounds__(kThreads) finalize_select_kernel(const Params 
   const int32_t r = blockIdx.x * kWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= P.B) return;  // whole warps leave together
+  grid_dep_wait();          // the row records come from the rows kernel
   const ReqInfo q = scan_request(P, r, lane);
   if (!q.ok) {
     if (lane == 0) raise_error(P, SV_DEVERR_LEN);

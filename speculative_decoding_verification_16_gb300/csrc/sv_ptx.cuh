@@ -1,9 +1,7 @@
 // sv_ptx.cuh -- thin inline-PTX wrappers used by the verify kernels (sm_103a).
 //
 // Bulk copies (cp.async.bulk) stream each CTA's slice of a logits row from
-// HBM into its own shared memory, completing on an mbarrier; cluster
-// barriers and distributed-shared-memory stores (mapa / st.shared::cluster)
-// exchange per-CTA partial results inside a thread-block cluster.
+// HBM into its own shared memory, completing on an mbarrier.
 #pragma once
 
 #include <cstdint>
@@ -101,57 +99,20 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// ---------------------------------------------------------------- clusters
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched as a programmatic dependent of the previous kernel on the
+// stream may start before that kernel ends; it must wait here before reading
+// anything the previous kernel writes.  Without the launch attribute the wait
+// returns at once.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-__device__ __forceinline__ uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void cluster_wait_acquire() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Address of the same shared-memory offset in CTA `rank` of this cluster.
-__device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-
-// 16-byte store into a cluster peer's shared memory that completes 16
-// transaction bytes on the peer's mbarrier `rbar` (both addresses from mapa).
-__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint32_t a, uint32_t b, uint32_t c,
-                                            uint32_t d, uint32_t rbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
-          raddr),
-      "r"(a), "r"(b), "r"(c), "r"(d), "r"(rbar)
-      : "memory");
-}
-
-__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+// Lets the dependent kernel of this one be scheduled as soon as every CTA of
+// this grid has executed it (the dependent still waits in grid_dep_wait for
+// this grid to finish and its writes to be visible).
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" :::);
 }
 
 // ---------------------------------------------------------------- math

@@ -67,8 +67,6 @@ constexpr int kMaxConsumerWarps = 24;
 constexpr int kPublishers = 2;
 constexpr int kGatherers = 4;
 static_assert(kMinStages >= kGatherers && kMinStages >= kPublishers, "stage reuse order");
-constexpr int kMaxSlices = 32;        // slices per row (gatherer lanes)
-constexpr int kPartWords = 16;        // 64-bit words per published partial (12 used)
 constexpr int kMaxSmemOffsets = 4096; // row_offsets entries kept in shared memory
 
 // Shared-memory header layout of the rows kernel (bytes from the base).
@@ -83,9 +81,6 @@ constexpr int kOffInfo = kOffStats + kMaxStages * 32;                   // [stag
 constexpr int kRowsHdrBytes = 12288;
 static_assert(kOffStatsBar + 8 * kMaxStages <= kOffPart, "rows kernel barriers");
 static_assert(kOffInfo + kMaxStages * 64 <= kRowsHdrBytes, "rows kernel header");
-
-// Partial / record word layout.
-enum { R_HT = 0, R_ST, R_MT, R_IT, R_HD, R_SD, R_MD, R_ID, R_BAD, R_XT, R_XD, R_HASX, R_NWORDS };
 
 struct RowInfo {
   int32_t g, k, r, off, off1, pair, gd;
@@ -600,6 +595,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
   const float sc = P.sc;
   uint64_t* parts = reinterpret_cast<uint64_t*>(P.parts);
   const uint64_t tagw = static_cast<uint64_t>(P.tag) << 32;
+  grid_dep_launch_dependents();  // the finalize kernel may take SMs this grid leaves
 
   // ---- set-up: row_offsets into shared memory (when they fit), barriers,
   //      the first NS units in flight
