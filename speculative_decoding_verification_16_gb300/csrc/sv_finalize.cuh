@@ -19,12 +19,21 @@
 // then read again from HBM and walked element by element with the mass left
 // over: running sums in (thread, element) order are sums in ascending token
 // id.  fp32 slice masses differ from the exact ones by a few 1e-7 in
-// probability, inside the near-tie margin the oracle reports.
+// probability, inside the near-tie margin the oracle reports.  A residual
+// mass below kZeroResidual counts as zero: the draw then uses p_t, as the
+// exact method does when max(0, p_t - p_d) vanishes.
 #pragma once
 
 #include "sv_common.cuh"
 
 namespace sv {
+
+// A residual mass sum max(0, p_t - p_d) below this is taken for zero (the
+// draw then uses p_t): the fp32 slice masses of two equal distributions
+// differ by rounding of order 1e-7, and a rejection with so little residual
+// mass happens with probability below it (it needs p_d(x) = 0 or p_t within
+// this of p_d everywhere).
+constexpr float kZeroResidual = 7.62939453125e-06f;  // 2^-17
 
 constexpr int kDrawThreads = 512;  // threads per CTA of the draw kernel
 constexpr int kDrawWarps = kDrawThreads / 32;
@@ -244,7 +253,7 @@ __global__ void __launch_bounds__(kDrawThreads) finalize_draw_kernel(const Param
     if (warp == sw) {  // choose the slice: first whose interval passes u * total
       float incl = warp_incl_scan(w);
       float total = __shfl_sync(0xffffffffu, incl, 31);
-      if (resid && !(total > 0.f)) {  // no residual mass (rounding only): draw from p_t
+      if (resid && !(total > kZeroResidual)) {  // no residual mass (rounding only): p_t
         resid = false;
         w = pk;
         incl = warp_incl_scan(w);

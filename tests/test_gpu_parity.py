@@ -36,14 +36,16 @@ def slice_len(L):
 
 
 def run_and_compare(cuda_lib, w, *, requests=None, T=None, top_k=None, top_p=None,
-                    want_conf=True, want_stats=True, mode=None, min_checked=1):
+                    want_conf=True, want_stats=True, mode=None, min_checked=1, max_len=None):
     spec = w.spec
     T = spec.temperature if T is None else T
     top_k = spec.top_k if top_k is None else top_k
     top_p = spec.top_p if top_p is None else top_p
     mode = w.mode if mode is None else mode
+    max_len = spec.max_len if max_len is None else max_len
     out = cuda_lib.verify_workload(w, want_conf=want_conf, want_stats=want_stats,
-                                   temperature=T, top_k=top_k, top_p=top_p, mode=mode)
+                                   temperature=T, top_k=top_k, top_p=top_p, mode=mode,
+                                   max_len=max_len)
     torch.cuda.synchronize()
     assert int(out.dev_error.item()) == 0
     requests = range(w.B) if requests is None else requests
@@ -119,6 +121,57 @@ def test_identical_rows_accept_all(cuda_lib):
     out, _ = run_and_compare(cuda_lib, w, min_checked=0)
     assert (out.accept_len.cpu() == 15).all()
     assert np.allclose(out.conf.cpu().numpy(), 1.0, atol=1e-5)
+
+
+def test_zero_residual_draws_from_target(cuda_lib):
+    """Identical target and draft rows, with the drafted token of position 5
+    masked (-inf) in both: p_d(x) = p_t(x) = 0 rejects it, the residual
+    max(0, p_t - p_d) is zero everywhere and the final token is drawn from
+    p_t of that row (the per-slice residual masses are rounding only, so the
+    draw drops them slice by slice before it falls back)."""
+    base = W.make_workload(W.WORKLOADS[2], W.SAMPLE, seed=41, device=DEV, B=5, V=12007)
+    offs = base.row_offsets.cpu().numpy()
+    t = base.target.clone()
+    d = torch.cat([t[offs[r]:offs[r + 1] - 1] for r in range(base.B)]).clone()
+    g = torch.Generator(device=DEV).manual_seed(3)
+    x = torch.multinomial(torch.softmax(d.float(), 1), 1, generator=g).flatten()
+    for r in range(base.B):
+        j = int(offs[r]) + 5
+        t[j, x[j - r]] = float("-inf")
+        d[j - r, x[j - r]] = float("-inf")
+    w = _pair_workload(t, d, x, [16] * base.B, base.uniforms)
+    for L in (None, 1000):
+        with slice_len(L):
+            out, _ = run_and_compare(cuda_lib, w)
+        assert (out.accept_len.cpu() == 5).all()
+
+
+@pytest.mark.parametrize("mode", [W.SAMPLE, W.GREEDY])
+def test_requests_longer_than_sixteen_rows(cuda_lib, mode):
+    """l_r up to 64 (the stopping row's slice masses are read after a_r is
+    known once a request has more rows than the draw kernel has warps)."""
+    lens = [40, 17, 1, 64, 2, 33]
+    w = W.make_workload(W.WORKLOADS[3], mode, seed=43, device=DEV, V=20011, lens=lens)
+    for L in (None, 1368):
+        with slice_len(L):
+            run_and_compare(cuda_lib, w, max_len=64)
+
+
+def test_long_requests_late_stop(cuda_lib):
+    """Identical rows accept every drafted token until position 30 of request
+    0, where the target masks the drafted token (a certain rejection and a
+    residual draw from row 30), and to the bonus row of the others."""
+    lens = [40, 33, 64]
+    base = W.make_workload(W.WORKLOADS[3], W.SAMPLE, seed=44, device=DEV, V=20011, lens=lens)
+    offs = base.row_offsets.cpu().numpy()
+    t = base.target.clone()
+    d = torch.cat([t[offs[r]:offs[r + 1] - 1] for r in range(base.B)]).clone()
+    g = torch.Generator(device=DEV).manual_seed(4)
+    x = torch.multinomial(torch.softmax(d.float(), 1), 1, generator=g).flatten()
+    t[30, x[30]] = float("-inf")
+    w = _pair_workload(t, d, x, lens, base.uniforms)
+    out, _ = run_and_compare(cuda_lib, w, max_len=64)
+    assert out.accept_len.cpu().tolist() == [30, 32, 63]
 
 
 def test_disjoint_supports(cuda_lib):
