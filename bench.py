@@ -268,11 +268,19 @@ def run_ours(args, world, rank, local):
     ws = L.alloc_workspace(B, Nt, dev)
     kw = dict(max_len=spec.max_len, temperature=spec.temperature, top_k=spec.top_k,
               top_p=spec.top_p, mode=mode, out=out, workspace=ws, stream=stream)
+    # unfiltered: one launch per step (the rows kernel finishes the requests
+    # in its tail), timed whole; filtered: the row kernel, timed alone, then
+    # the request kernel
+    filtered = (0 < spec.top_k < V) or spec.top_p < 1.0
     calls = []
     for s in sets:
         args_ = (s.target, s.draft, s.draft_tokens, s.uniforms, s.verify_lens, s.row_offsets)
-        calls.append((L.prepare("spec_verify_rows", *args_, **kw),
-                      L.prepare("spec_verify_finalize", *args_, **kw)))
+        if filtered:
+            calls.append((L.prepare("spec_verify_rows", *args_, **kw),
+                          L.prepare("spec_verify_finalize", *args_, **kw)))
+        else:
+            calls.append((L.prepare("spec_verify", *args_, **kw), lambda: None))
+    launches_per_step = 2 if filtered else 1
     # (sets use their own lengths; for ragged workloads the second set is
     # drawn with a different seed, so row counts may differ)
     n_rows = [s.n_target_rows + s.n_draft_rows for s in sets]
@@ -323,7 +331,6 @@ def run_ours(args, world, rank, local):
     peak, peak_src = hbm_peak()
     # the recorded traffic is for the full-size workload only
     traffic = recorded_traffic(spec.name) if args.requests <= 0 else None
-    filtered = (0 < spec.top_k < V) or spec.top_p < 1.0
 
     e2e = None
     if not args.no_e2e:
@@ -355,7 +362,7 @@ def run_ours(args, world, rank, local):
                          "mean_launch_ms": mean_rows_ms, "peak_source": peak_src},
             "hbm_gbs_step": bytes_per_launch / (elapsed_ms / K / 1e3) / 1e9,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
-            "gpu_launches": 2 * K,
+            "gpu_launches": launches_per_step * K,
         }
         print(json.dumps(line), flush=True)
 

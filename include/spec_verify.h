@@ -99,8 +99,11 @@ extern "C" {
 size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows);
 
 /*
- * The verify step: spec_verify_rows followed by spec_verify_finalize on the
- * same stream.
+ * The verify step: the work of spec_verify_rows followed by that of
+ * spec_verify_finalize on the same stream.  Unfiltered calls take one
+ * launch: the CTAs of the rows kernel finish the requests (the phase-2 work)
+ * themselves once their own slices are done and the rows of the request are
+ * complete everywhere.  Filtered calls take the two kernels.
  *
  *  target_logits  [N_t, V] device, dtype; 16-byte aligned base.
  *  draft_logits   [N_d, V] device, dtype; may be NULL when N_d == 0.
@@ -156,7 +159,9 @@ int spec_verify(const void* target_logits, const void* draft_logits,
  * once, slice by slice through shared memory; the CTAs holding the slices of
  * a row exchange partial statistics through the workspace, and the
  * per-row statistics, accept decisions and per-slice label partials go to
- * the workspace (row statistics also to out_row_stats when given).
+ * the workspace (row statistics also to out_row_stats when given).  In
+ * unfiltered sampling mode the per-slice sums of min(p_t, p_d) are formed
+ * even without out_conf: the final draw picks its slice from them.
  * Filtered: one CTA per row selects the kept set into the workspace.  This
  * is the bandwidth-bound phase.
  */

@@ -223,17 +223,12 @@ int check_args(const Args& a) {
   return SV_OK;
 }
 
-// Workspace layout: RowRec[N_t] | label partials float[N_t][32] | published
-// pass-1 partials uint64[N_t][32][16] (tag in the upper half of every word) |
-// filtered-path row records FiltRow[2 N_t] (N_t target rows, then the draft
-// rows).
-size_t ws_cpart_offset(int32_t n_target_rows) {
-  return (static_cast<size_t>(n_target_rows) * sizeof(RowRec) + 255) / 256 * 256;
-}
-
+// Workspace layout: RowRec[N_t] | published partials uint64[N_t][32][16]
+// (tag in the upper half of every word; pass-1 statistics, the label partial
+// and the row-record mark) | filtered-path row records FiltRow[2 N_t] (N_t
+// target rows, then the draft rows).
 size_t ws_parts_offset(int32_t n_target_rows) {
-  return ws_cpart_offset(n_target_rows) +
-         (static_cast<size_t>(n_target_rows) * kMaxSlices * sizeof(float) + 255) / 256 * 256;
+  return (static_cast<size_t>(n_target_rows) * sizeof(RowRec) + 255) / 256 * 256;
 }
 
 size_t ws_filt_offset(int32_t n_target_rows) {
@@ -266,8 +261,6 @@ Params make_params(const Args& a) {
   P.out_row_stats = a.out_row_stats;
   P.dev_error = a.dev_error;
   P.rec = static_cast<RowRec*>(a.workspace);
-  P.cpart = reinterpret_cast<float*>(static_cast<unsigned char*>(a.workspace) +
-                                     ws_cpart_offset(a.n_target_rows));
   P.parts = static_cast<unsigned char*>(a.workspace) + ws_parts_offset(a.n_target_rows);
   P.filt = static_cast<unsigned char*>(a.workspace) + ws_filt_offset(a.n_target_rows);
   return P;
@@ -329,7 +322,9 @@ int launch_rows(const Params& P, int smem, const DeviceCache& dc, bool need_z, b
 #undef SV_ROWS
 }
 
-int run_rows(const Args& a) {
+// fuse: the rows kernel also finishes the requests in its tail (unfiltered
+// path only; the caller then launches no finalize kernel).
+int run_rows(const Args& a, bool fuse) {
   DeviceCache dc;
   int rc = device_info(&dc);
   if (rc != SV_OK) return rc;
@@ -354,11 +349,14 @@ int run_rows(const Args& a) {
   P.tag = next_tag();
   P.offs_smem = geo.offs_smem;
   P.poll_ns = std::max(0, std::min(10000, env_int("SPEC_VERIFY_POLL_NS", 128)));
+  P.fuse = fuse ? 1 : 0;
   const int smem = geo.smem;
   // z is needed for sampling, labels and statistics; the exact max / argmax
   // only for greedy decisions and statistics
   const bool need_z = a.mode == SV_SAMPLE || a.out_conf != nullptr || a.out_row_stats != nullptr;
-  const bool need_conf = a.out_conf != nullptr;
+  // pass 2 (the per-slice sums of min(p_t, p_d)) for labels, and in sampling
+  // mode for the residual masses of the slices that the final draw picks from
+  const bool need_conf = a.out_conf != nullptr || a.mode == SV_SAMPLE;
   const bool track = a.mode == SV_GREEDY || a.out_row_stats != nullptr;
   // consumer warps (16 or 24) and, with labels, how many of them run pass 1
   // (SPEC_VERIFY_WARPS, SPEC_VERIFY_PASS1_WARPS)
@@ -402,6 +400,15 @@ int run_finalize(const Args& a, bool after_rows) {
                       after_rows, st);
 }
 
+// The whole step: unfiltered, one launch (the rows kernel finishes the
+// requests in its tail); filtered, the row kernel and then the request kernel
+// as its programmatic dependent.
+int run_call(const Args& a) {
+  const bool fuse = filter_k(a.V, a.top_k, a.top_p) == 0;
+  const int rc = run_rows(a, fuse);
+  return rc != SV_OK || fuse ? rc : run_finalize(a, true);
+}
+
 // ---------------------------------------------------------------- static scratch
 // Scratch of spec_verify_static: the same three workspace regions as a caller
 // workspace (row records, label partials, published pass-1 partials), sized
@@ -416,7 +423,6 @@ int run_finalize(const Args& a, bool after_rows) {
 constexpr size_t round256(size_t b) { return (b + 255) / 256 * 256; }
 constexpr size_t kStaticBytes =
     round256(round256(static_cast<size_t>(SV_STATIC_MAX_ROWS) * sizeof(RowRec)) +
-             round256(static_cast<size_t>(SV_STATIC_MAX_ROWS) * kMaxSlices * sizeof(float)) +
              static_cast<size_t>(SV_STATIC_MAX_ROWS) * kMaxSlices * kPartWords * 8 +
              static_cast<size_t>(SV_STATIC_MAX_ROWS) * 2 * sizeof(FiltRow)) +
     256;
@@ -473,7 +479,7 @@ size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows) {
 int spec_verify_rows(SV_ARGS_DECL) {
   SV_ARGS_PACK;
   const int rc = sv::check_args(a);
-  return rc != SV_OK ? rc : sv::run_rows(a);
+  return rc != SV_OK ? rc : sv::run_rows(a, false);
 }
 
 int spec_verify_finalize(SV_ARGS_DECL) {
@@ -485,9 +491,7 @@ int spec_verify_finalize(SV_ARGS_DECL) {
 int spec_verify(SV_ARGS_DECL) {
   SV_ARGS_PACK;
   int rc = sv::check_args(a);
-  if (rc == SV_OK) rc = sv::run_rows(a);
-  if (rc == SV_OK) rc = sv::run_finalize(a, true);
-  return rc;
+  return rc != SV_OK ? rc : sv::run_call(a);
 }
 
 int spec_verify_static(const void* target_logits, const void* draft_logits,
@@ -507,9 +511,7 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
   void* workspace = ws;
   SV_ARGS_PACK;
   rc = sv::check_args(a);
-  if (rc == SV_OK) rc = sv::run_rows(a);
-  if (rc == SV_OK) rc = sv::run_finalize(a, true);
-  return rc;
+  return rc != SV_OK ? rc : sv::run_call(a);
 }
 
 const char* spec_verify_status_string(int status) {

@@ -38,8 +38,22 @@ static_assert(sizeof(RowRec) == 32, "RowRec layout");
 // it (greedy or statistics only); x the logits at the drafted token when the
 // slice holds it.
 constexpr int kMaxSlices = 32;  // slices per row
-constexpr int kPartWords = 16;  // 64-bit words per published partial (12 used)
+constexpr int kPartWords = 16;  // 64-bit words per published partial (14 used)
 enum { R_HT = 0, R_ST, R_MT, R_IT, R_HD, R_SD, R_MD, R_ID, R_BAD, R_XT, R_XD, R_HASX, R_NWORDS };
+// Words written after the exchange: the slice's label partial sum of
+// min(p_t, p_d) (pass 2, pairs only), and in slice 0's record the row's
+// accept decision and device error bits (rec_mark), written with its RowRec.
+constexpr int R_CP = R_NWORDS;
+constexpr int R_REC = R_NWORDS + 1;
+static_assert(R_REC < kPartWords, "partial record");
+
+__device__ __forceinline__ uint32_t rec_mark(bool acc, int flags) {
+  return (acc ? 0x80000000u : 0u) | (static_cast<uint32_t>(flags) & 0x7fffffffu);
+}
+
+__device__ __forceinline__ const uint64_t* part_words(const void* parts, int32_t g, int32_t k) {
+  return static_cast<const uint64_t*>(parts) + (static_cast<size_t>(g) * kMaxSlices + k) * kPartWords;
+}
 
 struct Params {
   const unsigned char* tgt;
@@ -60,7 +74,6 @@ struct Params {
   float* out_row_stats;
   int32_t* dev_error;
   RowRec* rec;
-  float* cpart;      // [N_t][kMaxSlices] label partial of each (row, slice): sum of min(p_t, p_d)
   void* parts;       // [N_t][32][16] words: published pass-1 partials
   void* filt;        // filtered path: FiltRow per target row, then per draft row
   uint32_t tag;      // per-call tag of the published partials (never 0)
@@ -72,7 +85,60 @@ struct Params {
   int32_t offs_smem; // row_offsets copied into shared memory (B + 1 <= kMaxSmemOffsets)
   int32_t nw1;       // rows kernel, labels on: consumer warps running pass 1
   int32_t poll_ns;   // rows kernel: gatherer sleep between polls
+  int32_t fuse;      // rows kernel: finish the requests in its tail (no finalize launch)
 };
+
+// Partial statistics of a row: sum_v 2^(x_v * sc) = s * 2^h; m = max raw
+// logit and i = lowest id holding it (tracked variant only; m = -inf, i =
+// INT_MAX otherwise).
+struct RStat {
+  float h, s, m;
+  int32_t i;
+};
+
+__device__ __forceinline__ RStat rstat_empty() {
+  return RStat{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+}
+
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ float warp_sum_f32(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Merge two statistics (a target and a draft row) over the 32 lanes'
+// partials: max reference, one rescale each, plain sum (the two dependency
+// chains interleaved); with TRACK also the max and the lowest id holding it
+// (without TRACK those fields are unused and left as they are).  Every lane
+// gets the same bits.
+template <bool TRACK>
+__device__ __forceinline__ void rstat_warp_reduce2(RStat& a, RStat& b) {
+  const float ha = warp_max_f32(a.h), hb = warp_max_f32(b.h);
+  float sa = a.h == -INFINITY ? 0.f : a.s * ex2(a.h - ha);
+  float sb = b.h == -INFINITY ? 0.f : b.s * ex2(b.h - hb);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    sa += __shfl_xor_sync(0xffffffffu, sa, off);
+    sb += __shfl_xor_sync(0xffffffffu, sb, off);
+  }
+  a.s = ha == -INFINITY ? 0.f : sa;
+  b.s = hb == -INFINITY ? 0.f : sb;
+  a.h = ha;
+  b.h = hb;
+  if (TRACK) {
+    const float ma = warp_max_f32(a.m), mb = warp_max_f32(b.m);
+    a.i = __reduce_min_sync(0xffffffffu, a.m == ma ? a.i : 0x7fffffff);
+    b.i = __reduce_min_sync(0xffffffffu, b.m == mb ? b.i : 0x7fffffff);
+    a.m = ma;
+    b.m = mb;
+  }
+}
 
 __device__ __forceinline__ void raise_error(const Params& P, int bits) {
   if (P.dev_error != nullptr) atomicOr(P.dev_error, bits);

@@ -52,6 +52,7 @@
 #pragma once
 
 #include "sv_common.cuh"
+#include "sv_finalize.cuh"
 
 namespace sv {
 
@@ -74,13 +75,17 @@ constexpr int kOffFull = 0;                                   // kMaxStages mbar
 constexpr int kOffEmpty = kOffFull + 8 * kMaxStages;
 constexpr int kOffPartBar = kOffEmpty + 8 * kMaxStages;
 constexpr int kOffStatsBar = kOffPartBar + 8 * kMaxStages;
+constexpr int kOffTailBar = kOffStatsBar + 8 * kMaxStages;   // slice copies of the tail
 constexpr int kOffPart = 256;                                 // [stage][warp][16] words
 constexpr int kOffCp = kOffPart + kMaxStages * kMaxConsumerWarps * 64;  // [stage][warp] floats
 constexpr int kOffStats = kOffCp + kMaxStages * kMaxConsumerWarps * 4;  // [stage][8] words
 constexpr int kOffInfo = kOffStats + kMaxStages * 32;                   // [stage] RowInfo
+constexpr int kOffTail = kOffInfo + kMaxStages * 64;                    // DrawSel, then scratch
 constexpr int kRowsHdrBytes = 12288;
-static_assert(kOffStatsBar + 8 * kMaxStages <= kOffPart, "rows kernel barriers");
-static_assert(kOffInfo + kMaxStages * 64 <= kRowsHdrBytes, "rows kernel header");
+static_assert(kOffTailBar + 8 <= kOffPart, "rows kernel barriers");
+static_assert(sizeof(DrawSel) <= 64, "tail choice");
+static_assert(kOffCp - kOffPart >= 4 * SV_MAX_LEN, "tail row marks");
+static_assert(kOffTail + 64 + 4 * 32 <= kRowsHdrBytes, "rows kernel header");
 
 struct RowInfo {
   int32_t g, k, r, off, off1, pair, gd;
@@ -115,58 +120,6 @@ struct RingPos {
     }
   }
 };
-
-// Partial statistics of a row: sum_v 2^(x_v * sc) = s * 2^h; m = max raw
-// logit and i = lowest id holding it (tracked variant only; m = -inf, i =
-// INT_MAX otherwise).
-struct RStat {
-  float h, s, m;
-  int32_t i;
-};
-
-__device__ __forceinline__ RStat rstat_empty() {
-  return RStat{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
-}
-
-__device__ __forceinline__ float warp_max_f32(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
-}
-
-__device__ __forceinline__ float warp_sum_f32(float v) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  return v;
-}
-
-// Merge two statistics (a target and a draft row) over the 32 lanes'
-// partials: max reference, one rescale each, plain sum (the two dependency
-// chains interleaved); with TRACK also the max and the lowest id holding it
-// (without TRACK those fields are unused and left as they are).  Every lane
-// gets the same bits.
-template <bool TRACK>
-__device__ __forceinline__ void rstat_warp_reduce2(RStat& a, RStat& b) {
-  const float ha = warp_max_f32(a.h), hb = warp_max_f32(b.h);
-  float sa = a.h == -INFINITY ? 0.f : a.s * ex2(a.h - ha);
-  float sb = b.h == -INFINITY ? 0.f : b.s * ex2(b.h - hb);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    sa += __shfl_xor_sync(0xffffffffu, sa, off);
-    sb += __shfl_xor_sync(0xffffffffu, sb, off);
-  }
-  a.s = ha == -INFINITY ? 0.f : sa;
-  b.s = hb == -INFINITY ? 0.f : sb;
-  a.h = ha;
-  b.h = hb;
-  if (TRACK) {
-    const float ma = warp_max_f32(a.m), mb = warp_max_f32(b.m);
-    a.i = __reduce_min_sync(0xffffffffu, a.m == ma ? a.i : 0x7fffffff);
-    b.i = __reduce_min_sync(0xffffffffu, b.m == mb ? b.i : 0x7fffffff);
-    a.m = ma;
-    b.m = mb;
-  }
-}
 
 template <int VEC>
 __device__ __forceinline__ float vmax_nan(const float* x) {
@@ -570,12 +523,13 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
   asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
+
 __device__ __forceinline__ void named_bar_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 // Threads of the rows kernel: NCW consumer warps, producer, publishers, gatherers.
-constexpr int rows_threads(int ncw) { return (ncw + 1 + kPublishers + kGatherers) * 32; }
+__host__ __device__ constexpr int rows_threads(int ncw) { return (ncw + 1 + kPublishers + kGatherers) * 32; }
 
 template <int ES, int NCW, bool NEED_Z, bool NEED_CONF, bool TRACK>
 __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params P) {
@@ -618,6 +572,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         mbar_init(sm.partbar(s), NW1);
         mbar_init(sm.statsbar(s), 1);
       }
+      mbar_init(smem_addr(smem_raw + kOffTailBar), 1);
       fence_mbar_init();
     }
     if (lane < n_units) plan = plan_unit<ES>(P, offs, c + lane * N);
@@ -701,7 +656,8 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
           if (info.pair) {
             float cs = 0.f;
             for (int w = 0; w < NW2; ++w) cs += sm.cp(s)[w];
-            P.cpart[static_cast<size_t>(info.g) * kMaxSlices + info.k] = cs / sm.stats(s)[1];
+            uint64_t* dst = parts + (static_cast<size_t>(info.g) * kMaxSlices + info.k) * kPartWords;
+            st_relaxed_u64(dst + R_CP, tagw | __float_as_uint(cs / sm.stats(s)[1]));
           }
           mbar_arrive(sm.empty(s));
         }
@@ -875,6 +831,8 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         rr.mt = gt.h; rr.zt = gt.s; rr.md = gdr.h; rr.zd = gdr.s;
         rr.argt = gt.i; rr.acc = acc; rr.pick = -1; rr.flags = fl;
         P.rec[g] = rr;
+        st_relaxed_u64(parts + static_cast<size_t>(g) * kMaxSlices * kPartWords + R_REC,
+                       tagw | rec_mark(acc != 0, fl));
         if (TRACK && P.out_row_stats != nullptr) {
           // Z relative to the true max: s * 2^(h - m sc)
           float* o = P.out_row_stats + 3 * static_cast<size_t>(g);
@@ -895,6 +853,19 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
     }
   }
   if (timeout && lane == 0) raise_error(P, SV_DEVERR_TIMEOUT);
+  if (!P.fuse) return;
+  // ---- tail: every role has left its loop and every copy has been consumed,
+  //      so stage 0's buffers are free; this CTA finishes requests blockIdx.x,
+  //      blockIdx.x + gridDim.x, ... as soon as their rows are done elsewhere
+  //      (skipped after a timeout: the stages may still be in use)
+  if (__syncthreads_or(timeout ? 1 : 0)) return;
+  const FinishSmem fs{reinterpret_cast<DrawSel*>(smem_raw + kOffTail),
+                      reinterpret_cast<float*>(smem_raw + kOffTail + 64),
+                      reinterpret_cast<uint32_t*>(smem_raw + kOffPart),  // free after the loops
+                      sm.tbuf(0), sm.dbuf(0), smem_addr(smem_raw + kOffTailBar)};
+  uint32_t phase = 0;
+  for (int32_t r = c; r < P.B; r += N)
+    if (!finish_request<ES, rows_threads(NCW) / 32>(P, r, fs, true, phase)) break;
 }
 
 }  // namespace sv

@@ -215,6 +215,41 @@ def test_greedy_without_labels_or_stats(cuda_lib):
     run_and_compare(cuda_lib, w, want_conf=False, want_stats=False)
 
 
+def test_sampling_without_labels_or_stats(cuda_lib):
+    """The final draw takes its slice masses from pass 2 even when no labels
+    are asked for."""
+    for idx, V, B in ((2, 50000, 8), (3, 20011, 24), (0, None, None)):
+        w = W.make_workload(W.WORKLOADS[idx], W.SAMPLE, seed=11 + idx, device=DEV, B=B, V=V)
+        run_and_compare(cuda_lib, w, want_conf=False, want_stats=False)
+
+
+@pytest.mark.parametrize("mode", [W.SAMPLE, W.GREEDY])
+def test_split_entry_points(cuda_lib, mode):
+    """spec_verify_rows then spec_verify_finalize (the finalize kernels as
+    their own launches) against the oracle."""
+    cases = ((2, 30011, 6, None, None), (3, 20011, 24, None, 2000), (0, None, None, None, None),
+             (3, 9001, None, [40, 1, 17, 3], None))
+    for idx, V, B, lens, L in cases:
+        w = W.make_workload(W.WORKLOADS[idx], mode, seed=51 + idx, device=DEV, B=B, V=V, lens=lens)
+        max_len = max(16, int(w.verify_lens.max()))
+        for want_conf in (True, False):
+            out = cuda_lib.alloc_outputs(w.n_target_rows, w.B, DEV, want_conf=want_conf,
+                                         want_stats=True)
+            ws = cuda_lib.alloc_workspace(w.B, w.n_target_rows, DEV)
+            args = (w.target, w.draft, w.draft_tokens, w.uniforms, w.verify_lens, w.row_offsets)
+            kw = dict(max_len=max_len, temperature=w.spec.temperature, mode=mode, out=out,
+                      workspace=ws)
+            with slice_len(L):
+                cuda_lib.prepare("spec_verify_rows", *args, **kw)()
+                cuda_lib.prepare("spec_verify_finalize", *args, **kw)()
+            torch.cuda.synchronize()
+            assert int(out.dev_error.item()) == 0
+            ref = oracle_requests(w, range(w.B), mode=mode, temperature=w.spec.temperature,
+                                  top_k=0, top_p=1.0, want_conf=True)
+            n, n_tie = compare(w, out, ref, check_stats=True, check_conf=want_conf)
+            assert n - n_tie >= 1
+
+
 def test_hand_derived_cases_on_gpu(cuda_lib):
     path = os.path.join(os.path.dirname(__file__), "golden", "hand_cases.json")
     for case in json.load(open(path))["cases"]:
