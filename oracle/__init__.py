@@ -21,3 +21,8 @@ from .spec_verify_oracle import (  # noqa: F401
     verify_request,
     spec_verify_oracle,
 )
+from .dspark_schedule_oracle import (  # noqa: F401
+    prefix_survival,
+    schedule_prefix,
+    expected_tokens,
+)
