@@ -226,6 +226,37 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
                        float* out_conf, float* out_row_stats, int32_t* dev_error,
                        void* stream);
 
+/*
+ * DSpark hardware-aware prefix scheduler ("DeepSeek DSpark speculative
+ * decoding" tutorial, section "硬件感知前缀调度器"): the verify lengths l_r
+ * of a pool of B requests for the next step.  Drafted position k of request
+ * r carries a conditional survival probability c_{r,k} (section "置信度预测头";
+ * the verify step's own labels c* serve where no confidence head exists);
+ * its prefix survival is S_{r,k} = prod_{i<=k} c_{r,i}.  Every request starts
+ * at l_r = 1; candidates are added best S first (equal S: lower r, then
+ * lower k) while Theta = tau * SPS(B) strictly rises, with tau =
+ * sum_r (1 + sum_{k < l_r - 1} S_{r,k}) the expected tokens of the step and
+ * B = sum_r l_r; the scan also stops when the table has no SPS(B + 1).  One
+ * CTA, float64 throughout.
+ *
+ *  conf       [B][K] float32 device, row-major: c_{r,k} for k = 0..K-1 (the
+ *             first drafted position first); clamped to [0, 1], NaN as 0.
+ *             May be NULL when K == 0.
+ *  B, K       1 <= B, 0 <= K, B * K <= SV_SCHEDULE_MAX_CANDIDATES
+ *             (else SV_ERR_UNSUPPORTED).
+ *  sps        [n_sps] float64 device: SPS(b) for batch b = 0..n_sps-1 (the
+ *             target's steps per second at b verified tokens); n_sps > B.
+ *  out_lens   [B] int32 device: l_r in [1, K + 1].
+ *  out_theta  [2] float64 device or NULL: Theta of the schedule and the
+ *             number of candidates added.
+ *  stream     cudaStream_t; stream-ordered, no host synchronisation.
+ * Returns SV_OK, SV_ERR_ARG (null, misaligned or inconsistent arguments),
+ * SV_ERR_UNSUPPORTED or SV_ERR_CUDA.
+ */
+#define SV_SCHEDULE_MAX_CANDIDATES 8192
+int spec_verify_schedule(const float* conf, int32_t B, int32_t K, const double* sps,
+                         int32_t n_sps, int32_t* out_lens, double* out_theta, void* stream);
+
 /* Static text for a status code (host). */
 const char* spec_verify_status_string(int status);
 

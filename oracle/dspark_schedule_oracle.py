@@ -22,8 +22,8 @@ Readings where the pages are silent (each one is also listed in the design doc):
 
 * tau is the expected number of tokens one verify step produces: one per
   request (the replacement or bonus token) plus each verified draft k,
-  which is kept when drafts 1..k all pass, probability S_{r,k}.  So
-  tau = sum_r (1 + sum_{k < l_r} S_{r,k}).
+  which is kept when drafts 1..k all pass, probability S_{r,k}.  So, with
+  positions counted from k = 0, tau = sum_r (1 + sum_{k < l_r - 1} S_{r,k}).
 * l_r counts verified target rows (1 + drafted tokens verified), as in the
   verify step; every request starts at l_r = 1, so B starts at the number
   of requests and tau at the same number.  B = sum_r l_r.
@@ -58,7 +58,8 @@ def schedule_prefix(conf, sps):
     Returns a dict: ``lens`` int64 [B] in 1 .. K+1, ``theta`` (the final
     Theta), ``added`` (candidates added), ``margin`` (the smallest relative
     gap |Theta_next - Theta| / Theta over every comparison made, for
-    near-tie reporting).
+    near-tie reporting; comparisons whose outcome cannot depend on rounding
+    are left out).
     """
     S = prefix_survival(conf)
     B, K = S.shape
@@ -79,7 +80,10 @@ def schedule_prefix(conf, sps):
             break
         tau_next = tau + s
         theta_next = tau_next * sps[b + 1]
-        margin = min(margin, abs(theta_next - theta) / max(abs(theta), 1e-300))
+        # a zero-S candidate against a curve that does not rise leaves
+        # Theta_next <= Theta exactly in any arithmetic: not a near tie
+        if not (s == 0.0 and sps[b + 1] <= sps[b]):
+            margin = min(margin, abs(theta_next - theta) / max(abs(theta), 1e-300))
         if not theta_next > theta:
             break
         assert lens[r] == k + 1, "candidates of a request come as a prefix"

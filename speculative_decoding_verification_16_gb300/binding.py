@@ -48,6 +48,9 @@ _lib.spec_verify_status_string.argtypes = [ctypes.c_int]
 _lib.spec_verify_status_string.restype = ctypes.c_char_p
 _lib.spec_verify_slices_per_row.argtypes = [_i32, _i32, _i32, _f32]
 _lib.spec_verify_slices_per_row.restype = ctypes.c_int
+_lib.spec_verify_schedule.argtypes = [_vp, _i32, _i32, _vp, _i32, _vp, _vp, _vp]
+_lib.spec_verify_schedule.restype = ctypes.c_int
+SV_SCHEDULE_MAX_CANDIDATES = 8192
 
 
 class SpecVerifyError(RuntimeError):
@@ -206,3 +209,28 @@ def verify_workload(w, *, want_conf=True, want_stats=False, **kw) -> Outputs:
                        top_k=kw.pop("top_k", spec.top_k), top_p=kw.pop("top_p", spec.top_p),
                        mode=kw.pop("mode", w.mode), want_conf=want_conf, want_stats=want_stats,
                        **kw)
+
+
+def spec_verify_schedule(conf: torch.Tensor, sps: torch.Tensor, *, out_lens=None,
+                         out_theta=None, stream=None):
+    """DSpark prefix schedule of a pool: ``conf`` [B, K] float32 (survival
+    probability of each drafted position), ``sps`` [n] float64 (steps per
+    second at each batch size).  Returns (lens int32 [B], theta float64 [2]:
+    Theta and the number of candidates added), all on the device."""
+    assert conf.dim() == 2 and conf.dtype == torch.float32 and conf.is_contiguous()
+    assert sps.dim() == 1 and sps.dtype == torch.float64 and sps.is_contiguous()
+    B, K = conf.shape
+    dev = conf.device
+    if out_lens is None:
+        out_lens = torch.empty(B, dtype=torch.int32, device=dev)
+    if out_theta is None:
+        out_theta = torch.empty(2, dtype=torch.float64, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    rc = _lib.spec_verify_schedule(_ptr(conf) if conf.numel() else None, _i32(B), _i32(K),
+                                   _ptr(sps), _i32(sps.numel()), _ptr(out_lens),
+                                   _ptr(out_theta), ctypes.c_void_p(stream.cuda_stream))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc)
+    return out_lens, out_theta
+

@@ -19,6 +19,7 @@
 #include "sv_filter.cuh"
 #include "sv_finalize.cuh"
 #include "sv_rows.cuh"
+#include "sv_schedule.cuh"
 
 namespace sv {
 namespace {
@@ -132,8 +133,8 @@ void remember_prepared(int dev, const void* fn, int smem, int C, int status) {
 // dependent of the previous kernel on the stream, which then must be this
 // library's rows kernel of the same call (the kernel reads only the call's
 // inputs before grid_dep_wait, and the rows kernel writes none of them).
-template <typename K>
-int launch_plain(K kernel, const Params& P, int grid, int threads, int smem, int max_smem,
+template <typename K, typename Arg>
+int launch_plain(K kernel, const Arg& P, int grid, int threads, int smem, int max_smem,
                  bool dependent, cudaStream_t stream) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
@@ -512,6 +513,27 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
   SV_ARGS_PACK;
   rc = sv::check_args(a);
   return rc != SV_OK ? rc : sv::run_call(a);
+}
+
+int spec_verify_schedule(const float* conf, int32_t B, int32_t K, const double* sps,
+                         int32_t n_sps, int32_t* out_lens, double* out_theta, void* stream) {
+  using sv::aligned;
+  if (B < 1 || K < 0 || n_sps <= B || sps == nullptr || out_lens == nullptr ||
+      (K > 0 && conf == nullptr))
+    return SV_ERR_ARG;
+  if ((conf != nullptr && !aligned(conf, 4)) || !aligned(sps, 8) || !aligned(out_lens, 4) ||
+      (out_theta != nullptr && !aligned(out_theta, 8)))
+    return SV_ERR_ARG;
+  const int64_t n = static_cast<int64_t>(B) * K;
+  if (n > SV_SCHEDULE_MAX_CANDIDATES || B > SV_SCHEDULE_MAX_CANDIDATES) return SV_ERR_UNSUPPORTED;
+  sv::DeviceCache dc;
+  const int rc = sv::device_info(&dc);
+  if (rc != SV_OK) return rc;
+  sv::ScheduleArgs A{conf, B, K, sps, n_sps, out_lens, out_theta,
+                     static_cast<int32_t>(std::max<int64_t>(2, (n + 1) & ~int64_t{1}))};
+  const int smem = A.npad * (2 * 8 + 2 * 2) + ((B + 1) & ~1) * 4 + sv::kScheduleWarps * (2 * 8 + 4);
+  return sv::launch_plain(sv::schedule_kernel, A, 1, sv::kScheduleThreads, smem, dc.max_smem_optin,
+                          false, static_cast<cudaStream_t>(stream));
 }
 
 const char* spec_verify_status_string(int status) {

@@ -122,3 +122,21 @@ def test_static_entry_rejects_oversized_problem_before_any_device_call(lib):
     for nt, code in ((4097, -6), (8192, -6)):
         assert f(fake, fake, fake, fake, fake, fake, B, 151936, nt, max_len, 0, 1.0, 0, 1.0, 1,
                  fake, fake, fake, None, None, None) == code
+
+
+def test_schedule_rejects_bad_host_arguments(lib):
+    """spec_verify_schedule checks its arguments on the host (fake pointers,
+    never dereferenced: every call below must be refused first)."""
+    f = lib.spec_verify_schedule
+    f.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                  ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    p, q = 0x10000, 0x20000
+    assert f(p, 0, 4, q, 10, p, None, None) == -1            # B < 1
+    assert f(p, 4, -1, q, 10, p, None, None) == -1           # K < 0
+    assert f(p, 4, 3, q, 4, p, None, None) == -1             # no SPS entry beyond B
+    assert f(None, 4, 3, q, 10, p, None, None) == -1         # conf missing
+    assert f(p, 4, 3, None, 10, p, None, None) == -1         # sps missing
+    assert f(p, 4, 3, q, 10, None, None, None) == -1         # out_lens missing
+    assert f(p, 4, 3, q + 4, 10, p, None, None) == -1        # sps not 8-byte aligned
+    assert f(p, 1000, 9, q, 10000, p, None, None) == -4      # above SV_SCHEDULE_MAX_CANDIDATES
