@@ -1,9 +1,11 @@
 #!/usr/bin/env python
 """Benchmark of the GB300 verify step.
 
-One step = one pass of the whole verify path (rows kernel + finalize kernel:
-statistics, c* labels, accept test, first-rejection cut, replacement / bonus
-draw) over one batch of the synthetic workload, inputs resident in HBM.
+One step = one pass of the whole verify path (statistics, c* labels, accept
+test, first-rejection cut, replacement / bonus draw) over one batch of the
+synthetic workload, inputs resident in HBM: one launch of the rows kernel,
+which finishes the requests in its tail (filtered workloads: the row kernel
+and the request kernel).
 Default workload: B = 32 requests, block 16 (15 drafted positions + bonus),
 V = 151,936, bf16 logits, T = 1 sampling with labels -- the workload on which
 the 70%-of-HBM goal is stated.
@@ -11,13 +13,20 @@ the 70%-of-HBM goal is stated.
 Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
 and torch.cuda.synchronize(); CUDA events on the launch stream.  Two copies of
 the inputs (2 x 301 MB, each larger than the 129 MB L2) alternate between
-steps.  The rows kernel is additionally bracketed by events each step to give
-its own duration for the roofline.  Multi-GPU: one process per GPU, each
+steps.  The step's launch (filtered: the row kernel) is additionally
+bracketed by events each step to give its own duration for the roofline.
+Multi-GPU: one process per GPU, each
 verifying its own independent batch (requests are independent units; no
 collective on the data path), time = max over ranks.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload I] [--mode sample|greedy]
+
+--component schedule prints one line for the DSpark prefix scheduler instead
+(spec_verify_schedule on a pool of 256 requests x 15 positions whose
+confidences are the verify step's own labels on the ragged workload; the
+SPS curve is synthetic: flat to 1,024 tokens, then falling as 1/B), with the
+fp64 oracle timed beside it.
 """
 
 import os
@@ -59,6 +68,7 @@ def parse():
                          "(small cases for profiling; the timed default keeps B)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--component", choices=("verify", "schedule"), default="verify")
     return ap.parse_args()
 
 
@@ -408,10 +418,75 @@ def run_e2e(L, w, spec, mode, dev, stream, kw, K, world):
             "steps": steps}
 
 
+def run_schedule(args, rank):
+    """DSpark prefix scheduler: schedules per second on a 256 x 15 pool."""
+    import numpy as np
+
+    from speculative_decoding_verification_16_gb300 import binding as L
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    spec = W.WORKLOADS[3]  # ragged, B = 256, block 16
+    w = W.make_workload(spec, W.SAMPLE, seed=3000, device=dev)
+    out = L.verify_workload(w)
+    torch.cuda.synchronize()
+    K = spec.max_len - 1
+    conf = torch.zeros((w.B, K), dtype=torch.float32, device=dev)
+    lens = w.verify_lens.cpu().tolist()
+    offs = w.row_offsets.cpu().tolist()
+    for r in range(w.B):  # drafted positions of request r; missing ones stay 0
+        n = lens[r] - 1
+        if n > 0:
+            conf[r, :n] = out.conf[offs[r] - r:offs[r] - r + n]
+    b = np.arange(w.B * (K + 1) + 2, dtype=np.float64)
+    sps_np = 1e4 / np.maximum(1024.0, b)
+    sps = torch.tensor(sps_np, device=dev)
+    out_lens = torch.empty(w.B, dtype=torch.int32, device=dev)
+    theta = torch.empty(2, dtype=torch.float64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        L.spec_verify_schedule(conf, sps, out_lens=out_lens, out_theta=theta, stream=stream)
+    torch.cuda.synchronize()
+    K_steps = min(args.steps, 2000)
+    a, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K_steps):
+        L.spec_verify_schedule(conf, sps, out_lens=out_lens, out_theta=theta, stream=stream)
+    e.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(e) / K_steps
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        t0, n = time.perf_counter(), 0
+        c_np = conf.cpu().numpy()
+        while time.perf_counter() - t0 < 5.0 or n == 0:
+            oracle.schedule_prefix(c_np, sps_np)
+            n += 1
+        cpu = {"value": n / (time.perf_counter() - t0), "unit": "schedules/s", "cores": 1,
+               "kind": "oracle", "sample": f"{n} schedules of the same pool, 5 s of one core"}
+    if rank == 0:
+        print(json.dumps({
+            "metric": "DSpark prefix schedules/s (256 requests x 15 positions)",
+            "value": 1e3 / ms, "unit": "schedules/s", "n_gpus": 1, "steps": K_steps,
+            "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "dspark_pool_b256_k15",
+                       "confidences": "verify labels c* of dspark_ragged_b256_v129280",
+                       "sps": "synthetic: 1e4 / max(1024, B)",
+                       "added": int(theta[1].item()), "theta": float(theta[0].item())},
+            "roofline": {"bound": "latency", "achieved": None, "peak": None, "unit": None,
+                         "frac": None, "traffic": None, "kernel": "schedule_kernel"},
+            "cpu_baseline": cpu, "gpu_launches": K_steps,
+        }), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup()
-    if args.impl == "reference":
+    if args.component == "schedule":
+        run_schedule(args, rank)
+    elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
         run_ours(args, world, rank, local)
