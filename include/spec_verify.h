@@ -77,7 +77,7 @@ extern "C" {
 #define SV_ERR_ARG (-1)         /* null/misaligned pointer, bad size or parameter */
 #define SV_ERR_DTYPE (-2)       /* dtype is neither SV_BF16 nor SV_FP32 */
 #define SV_ERR_CUDA (-3)        /* a CUDA runtime call or a launch failed */
-#define SV_ERR_UNSUPPORTED (-4) /* kept set above SV_MAX_FILTER_K tokens, or a shape not served */
+#define SV_ERR_UNSUPPORTED (-4) /* a shape the kernels do not take */
 #define SV_ERR_WORKSPACE (-5)   /* workspace missing, misaligned or too small */
 #define SV_ERR_TOO_LARGE (-6)   /* spec_verify_static: more than SV_STATIC_MAX_ROWS rows */
 
@@ -89,7 +89,7 @@ extern "C" {
 
 /* limits */
 #define SV_MAX_LEN 256       /* largest accepted max_len */
-#define SV_MAX_FILTER_K 64   /* largest top_k served together with top_p < 1 */
+#define SV_MAX_FILTER_K 64   /* largest kept set of the small kept-set path */
 #define SV_STATIC_MAX_ROWS 4096 /* largest n_target_rows of spec_verify_static */
 
 /*
@@ -121,13 +121,14 @@ size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows);
  *  temperature    T > 0 (required in sampling mode and whenever out_conf or
  *                 out_row_stats is requested; otherwise ignored).
  *  top_k          <= 0 or >= V: off.  Else keep the top_k tokens.
- *  top_p          in (0, 1]; 1 = off.  With either filter on, the kept set
- *                 (top_k if on, else V) must be at most SV_MAX_FILTER_K
- *                 tokens, else SV_ERR_UNSUPPORTED (full-vocabulary top-p
- *                 over V > 64 and top_k in (SV_MAX_FILTER_K, V) are not
- *                 served).  Filtered calls run the top-k path: one pass per
- *                 row selects the kept set exactly, then one warp per
- *                 request decides on the kept sets.
+ *  top_p          in (0, 1]; 1 = off.  Filtered calls whose kept set is at
+ *                 most SV_MAX_FILTER_K tokens (top_k <= 64 on) run the small
+ *                 kept-set path: one pass per row selects the set exactly,
+ *                 then one warp per request decides on it.  Larger kept
+ *                 sets (top_k above 64, or top_p over the whole vocabulary)
+ *                 run the general path: per row a bisection over the value
+ *                 key with exact fixed-point mass sums finds the kept set's
+ *                 threshold, then one CTA per request decides and draws.
  *  mode           SV_GREEDY or SV_SAMPLE.
  *  out_tokens     [N_t] int32 device: for request r, entries off_r .. off_r
  *                 + a_r - 1 = accepted drafts, entry off_r + a_r = the final

@@ -20,6 +20,7 @@
 #include "sv_finalize.cuh"
 #include "sv_rows.cuh"
 #include "sv_schedule.cuh"
+#include "sv_gfilter.cuh"
 
 namespace sv {
 namespace {
@@ -62,7 +63,7 @@ int round_up(int v, int m) { return (v + m - 1) / m * m; }
 int rowbuf_bytes(int S, int es) { return round_up(S * es + 32, 128); }
 
 // Size k of the kept set under top-k / top-p filtering: 0 when unfiltered,
-// -1 when the set can exceed SV_MAX_FILTER_K tokens (not served).
+// -1 when the set can exceed SV_MAX_FILTER_K tokens (the general path).
 int filter_k(int V, int top_k, float top_p) {
   const bool use_k = top_k > 0 && top_k < V;
   const bool use_p = top_p < 1.0f;
@@ -220,7 +221,6 @@ int check_args(const Args& a) {
   if (a.workspace == nullptr || !aligned(a.workspace, 256) ||
       a.workspace_bytes < spec_verify_workspace_size(a.B, a.n_target_rows))
     return SV_ERR_WORKSPACE;
-  if (filter_k(a.V, a.top_k, a.top_p) < 0) return SV_ERR_UNSUPPORTED;
   return SV_OK;
 }
 
@@ -253,7 +253,11 @@ Params make_params(const Args& a) {
   const bool need_t = a.mode == SV_SAMPLE || a.out_conf != nullptr || a.out_row_stats != nullptr;
   P.T = need_t ? a.temperature : 1.f;
   P.sc = static_cast<float>(1.4426950408889634 / static_cast<double>(P.T));
-  P.top_k = std::max(0, filter_k(a.V, a.top_k, a.top_p));  // > 0: filtered path
+  // the filtered paths: small kept sets (top_k = k <= SV_MAX_FILTER_K), or
+  // any size (gfilter: top_k as given, 0 = off, with P.gfilter set)
+  const int fk = filter_k(a.V, a.top_k, a.top_p);
+  P.gfilter = fk < 0;
+  P.top_k = fk >= 0 ? fk : (a.top_k > 0 && a.top_k < a.V ? a.top_k : 0);
   P.top_p = a.top_p;
   P.mode = a.mode;
   P.out_tokens = a.out_tokens;
@@ -332,6 +336,11 @@ int run_rows(const Args& a, bool fuse) {
   Params P = make_params(a);
   const int es = a.dtype == SV_BF16 ? 2 : 4;
   cudaStream_t st = static_cast<cudaStream_t>(a.stream);
+  if (P.gfilter) {  // kept sets of any size: bisection on the value key per row
+    const int rows = std::max(1, std::min(a.n_target_rows, dc.sms * 3));
+    if (es == 2) return launch_plain(gfilter_rows_kernel<2>, P, rows, kGThreads, 0, dc.max_smem_optin, false, st);
+    return launch_plain(gfilter_rows_kernel<4>, P, rows, kGThreads, 0, dc.max_smem_optin, false, st);
+  }
   if (P.top_k > 0) {  // top-k / top-p: one streaming pass per row, no exchange
     const int rows = P.Nt + P.Nd;
     const int grid = std::max(1, std::min(rows, dc.sms * kFilterCtasPerSm));
@@ -380,6 +389,13 @@ int run_finalize(const Args& a, bool after_rows) {
   const int es = a.dtype == SV_BF16 ? 2 : 4;
   cudaStream_t st = static_cast<cudaStream_t>(a.stream);
   const int per_warp_grid = (a.B + kWarps - 1) / kWarps;
+  if (P.gfilter) {  // kept sets of any size: one CTA per request
+    if (es == 2)
+      return launch_plain(gfilter_requests_kernel<2>, P, a.B, kGThreads, 0, dc.max_smem_optin,
+                          after_rows, st);
+    return launch_plain(gfilter_requests_kernel<4>, P, a.B, kGThreads, 0, dc.max_smem_optin,
+                        after_rows, st);
+  }
   if (P.top_k > 0)  // top-k / top-p: decisions on the kept sets, one warp per request
     return launch_plain(filter_requests_kernel, P, per_warp_grid, kThreads, 0, dc.max_smem_optin,
                         after_rows, st);
@@ -543,7 +559,7 @@ const char* spec_verify_status_string(int status) {
     case SV_ERR_DTYPE: return "unknown logits dtype";
     case SV_ERR_CUDA: return "CUDA runtime or launch failure";
     case SV_ERR_UNSUPPORTED:
-      return "not served: kept set above SV_MAX_FILTER_K tokens, or a shape the kernels do not take";
+      return "not served: a shape the kernels do not take";
     case SV_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
     case SV_ERR_TOO_LARGE:
       return "problem larger than the static scratch of spec_verify_static "

@@ -67,6 +67,7 @@ struct Params {
   float sc;       // log2(e) / T
   int32_t top_k;  // 0 = off
   float top_p;    // 1 = off
+  int32_t gfilter;  // kept sets of any size (top_k above SV_MAX_FILTER_K, or full-vocabulary top_p)
   int32_t mode;
   int32_t* out_tokens;
   int32_t* out_accept_len;
