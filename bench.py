@@ -69,6 +69,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--component", choices=("verify", "schedule"), default="verify")
+    ap.add_argument("--top-k", type=int, default=None, help="override the workload's top_k")
+    ap.add_argument("--top-p", type=float, default=None, help="override the workload's top_p")
     return ap.parse_args()
 
 
@@ -188,7 +190,7 @@ def recorded_traffic(workload_name):
 
 
 # --------------------------------------------------------------------- oracle (CPU legs)
-def oracle_rate(w, spec, mode, budget_s, ell_cap=None, start=0):
+def oracle_rate(w, spec, mode, budget_s, ell_cap=None, start=0, top_k=None, top_p=None):
     """Time the fp64 oracle on requests of ``w`` -- each cut to at most
     ``ell_cap`` target rows (a shorter request is itself a valid verify
     problem) -- until ``budget_s`` of oracle time has elapsed (at least one
@@ -215,7 +217,8 @@ def oracle_rate(w, spec, mode, budget_s, ell_cap=None, start=0):
         t0 = time.perf_counter()
         oracle.verify_request(oracle.decode_logits(t, dt),
                               oracle.decode_logits(d, dt).reshape(ell - 1, -1), x, u,
-                              spec.temperature, spec.top_k, spec.top_p, mode, want_conf=True)
+                              spec.temperature, spec.top_k if top_k is None else top_k,
+                              spec.top_p if top_p is None else top_p, mode, want_conf=True)
         secs += time.perf_counter() - t0
         pos += ell - 1
         nreq += 1
@@ -276,12 +279,17 @@ def run_ours(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     out = L.alloc_outputs(Nt, B, dev, want_conf=True)
     ws = L.alloc_workspace(B, Nt, dev)
-    kw = dict(max_len=spec.max_len, temperature=spec.temperature, top_k=spec.top_k,
-              top_p=spec.top_p, mode=mode, out=out, workspace=ws, stream=stream)
+    top_k = spec.top_k if args.top_k is None else args.top_k
+    top_p = spec.top_p if args.top_p is None else args.top_p
+    kw = dict(max_len=spec.max_len, temperature=spec.temperature, top_k=top_k,
+              top_p=top_p, mode=mode, out=out, workspace=ws, stream=stream)
     # unfiltered: one launch per step (the rows kernel finishes the requests
     # in its tail), timed whole; filtered: the row kernel, timed alone, then
     # the request kernel
-    filtered = (0 < spec.top_k < V) or spec.top_p < 1.0
+    filtered = (0 < top_k < V) or top_p < 1.0
+    # kept sets of at most 64 tokens take the small-set row kernel
+    row_kernel = ("filter_rows_kernel" if 0 < top_k <= 64 else "gfilter_rows_kernel") \
+        if filtered else "rows_kernel"
     calls = []
     for s in sets:
         args_ = (s.target, s.draft, s.draft_tokens, s.uniforms, s.verify_lens, s.row_offsets)
@@ -348,7 +356,7 @@ def run_ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, pos, secs, nreq = oracle_rate(w, spec, mode, 10.0)
+        rate, pos, secs, nreq = oracle_rate(w, spec, mode, 10.0, top_k=top_k, top_p=top_p)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{nreq} whole requests ({pos} drafted positions) of the same "
                          f"workload, {secs:.1f} s of single-thread fp64 oracle time"}
@@ -360,14 +368,14 @@ def run_ours(args, world, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": spec.name, "B": B, "block": spec.max_len, "V": V,
                        "logits": spec.dtype, "mode": args.mode,
-                       "temperature": spec.temperature, "top_k": spec.top_k,
-                       "top_p": spec.top_p, "labels": True,
+                       "temperature": spec.temperature, "top_k": top_k,
+                       "top_p": top_p, "labels": True,
                        "l2": f"inputs larger than L2: {len(sets)} input sets of "
                              f"{bytes_per_launch / 1e6:.0f} MB alternate between steps",
                        "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "filter_rows_kernel" if filtered else "rows_kernel",
+                         "kernel": row_kernel,
                          "bytes_per_launch": bytes_per_launch,
                          "mean_launch_ms": mean_rows_ms, "peak_source": peak_src},
             "hbm_gbs_step": bytes_per_launch / (elapsed_ms / K / 1e3) / 1e9,

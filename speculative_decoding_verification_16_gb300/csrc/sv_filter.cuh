@@ -35,7 +35,7 @@ namespace sv {
 
 constexpr int kMaxK = SV_MAX_FILTER_K;  // 64
 constexpr int kCandCap = 2 * kMaxK;     // per-warp candidate buffer
-constexpr int kFilterCtasPerSm = 4;
+constexpr int kFilterCtasPerSm = 6;
 
 struct FiltRow {
   int32_t n;       // kept tokens (<= k)
@@ -112,7 +112,7 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const unsigned char* p) {
 template <int ES>
 __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel(const Params P) {
   constexpr int VEC = 16 / ES;
-  constexpr int UNROLL = 4;
+  constexpr int UNROLL = 1;  // a short loop body: the kernel is bound by instruction supply
   __shared__ uint64_t cand[kWarps][kCandCap];
   __shared__ uint64_t merged[kWarps * kMaxK];
   __shared__ __align__(16) uint64_t bar_sh[kWarps];  // each warp's k-th best key
@@ -147,10 +147,12 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
     bool bad = false;
     // the loop runs on the warp's first vector, so that every lane takes
     // part in the warp-wide votes below; lanes past the end hold no element
-    for (int32_t kw = warp * 32; kw < nv; kw += UNROLL * kThreads) {
+    int iter = 0;
+    for (int32_t kw = warp * 32; kw < nv; kw += UNROLL * kThreads, ++iter) {
       // any warp's k-th best key bars the whole CTA: an element below it
       // cannot be among the CTA's k best, so the highest of them is used
-      {
+      // (read every fourth step: a stale bar only lets more vectors through)
+      if ((iter & 3) == 0) {
         uint64_t b = thr;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) b = max(b, bar_sh[w]);
@@ -169,20 +171,27 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
       for (int q = 0; q < UNROLL; ++q) {
         const int32_t k = kw + lane + q * kThreads;
         if (kw + q * kThreads >= nv) break;  // warp-uniform
-        float x[VEC];
         const uint32_t wv[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+        // screen: a vector whose largest logit is below the warp's bar holds
+        // no candidate (a NaN maximum goes on to the exact path and is
+        // flagged); bf16 vectors take their maximum on the packed pairs
+        float vm;
+        if (ES == 2) {
+          const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(wv[0], wv[1]),
+                                             bf16x2_max_nan(wv[2], wv[3]));
+          vm = fmax_nan(bf16lo(m2), bf16hi(m2));
+        } else {
+          vm = fmax_nan(fmax_nan(__uint_as_float(wv[0]), __uint_as_float(wv[1])),
+                        fmax_nan(__uint_as_float(wv[2]), __uint_as_float(wv[3])));
+        }
+        const bool maybe = k < nv && !(vm < thr_val);
+        if (!__any_sync(0xffffffffu, maybe)) continue;
+        float x[VEC];
 #pragma unroll
         for (int l = 0; l < VEC; ++l)
           x[l] = ES == 2 ? ((l & 1) ? bf16hi(wv[l >> 1]) : bf16lo(wv[l >> 1]))
                          : __uint_as_float(wv[l]);
         const int32_t i0 = k * VEC - s.hoff;
-        // screen: a vector whose largest logit is below the warp's bar holds
-        // no candidate (a NaN maximum goes on to the exact path and is flagged)
-        float vm = x[0];
-#pragma unroll
-        for (int l = 1; l < VEC; ++l) vm = fmax_nan(vm, x[l]);
-        const bool maybe = k < nv && !(vm < thr_val);
-        if (!__any_sync(0xffffffffu, maybe)) continue;
         // this lane's keys above the bar (NaN and +inf are flagged, not kept)
         uint64_t key[VEC];
         int c = 0;

@@ -116,6 +116,13 @@ __device__ __forceinline__ void grid_dep_launch_dependents() {
 }
 
 // ---------------------------------------------------------------- math
+// Lane-wise maximum of two bf16 pairs; a NaN in either input gives NaN.
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
 // Hardware base-2 exponential (MUFU); ex2(-inf) = +0.
 __device__ __forceinline__ float ex2(float x) {
   float y;
