@@ -337,7 +337,7 @@ int run_rows(const Args& a, bool fuse) {
   const int es = a.dtype == SV_BF16 ? 2 : 4;
   cudaStream_t st = static_cast<cudaStream_t>(a.stream);
   if (P.gfilter) {  // kept sets of any size: bisection on the value key per row
-    const int rows = std::max(1, std::min(a.n_target_rows, dc.sms * 3));
+    const int rows = std::max(1, std::min(a.n_target_rows, dc.sms * 2));  // 2 CTAs per SM
     if (es == 2) return launch_plain(gfilter_rows_kernel<2>, P, rows, kGThreads, 0, dc.max_smem_optin, false, st);
     return launch_plain(gfilter_rows_kernel<4>, P, rows, kGThreads, 0, dc.max_smem_optin, false, st);
   }

@@ -10,14 +10,16 @@
 // t and an id, the set being the tokens above t plus the tokens at t up to
 // that id.
 //
-// The threshold is found by bisection over the value key (16 bits for bf16,
-// 32 for fp32), one pass over the row per probe.  A probe counts the tokens
-// at or above it and sums their weights w = exp2(x sc - h) (h = x_max sc) as
+// The top-k threshold is found by bisection over the value key (16 bits for
+// bf16, 32 for fp32), one counting pass per probe; the top-p threshold by a
+// radix select, one pass per 8-bit digit: a histogram of counts and of
+// weights w = exp2(x sc - h) (h = x_max sc) over the elements that match the
+// digits chosen so far, then the bin where the cumulative mass from the top
+// reaches the target.  Weights are summed as
 // fixed-point integers of 2^-40, so every sum is exact and the same in any
-// order; weights are formed only for tokens at or above the probe.  Inside
-// the tie class of the final value, the cut falls after c tokens of equal
-// weight, c from integer arithmetic; a counting pass finds the id of the
-// c-th.
+// order.  Inside the tie class of the final value, the cut falls after c
+// tokens of equal weight, c from integer arithmetic; a counting pass finds
+// the id of the c-th.
 //
 //  gfilter_rows_kernel      one CTA per target row: the kept sets of the row
 //                           and of its draft partner, the label
@@ -208,11 +210,124 @@ __device__ __forceinline__ int32_t g_tie_id(const unsigned char* row, int32_t V,
   return id;
 }
 
+constexpr int kHCopies = 8;  // histogram copies (two warps share one)
+
+// Shared histograms of one radix level: per copy 256 bins of a count and a
+// fixed-point mass.
+struct GHist {
+  uint32_t cnt[kHCopies][256];
+  unsigned long long mass[kHCopies][256];
+};
+
+// The value key t of the first element, in (value desc, id asc) order, at
+// which the cumulative count (by_mass false) or fixed-point mass reaches
+// `target` (>= 1, at most the row's total), with the count and mass of the
+// keys above t and the count and total weight of the keys equal to t (the
+// top-p search; top-k counts by bisection, which needs no weights).  One
+// pass per 8-bit digit of the key (two for bf16, four for fp32): a histogram
+// of the elements that match the digits chosen so far, then the bin where
+// the target falls.
+struct GSel {
+  uint32_t t;
+  unsigned long long n_above, m_above, ties, m_ties;
+};
+
+template <int ES>
+__device__ __forceinline__ GSel g_radix_select(const unsigned char* row, int32_t V, float sc, float h,
+                                               unsigned long long target, bool by_mass,
+                                               GHist* hist, unsigned long long* red) {
+  constexpr int W = ES == 2 ? 16 : 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int copy = warp % kHCopies;
+  uint32_t prefix = 0;
+  unsigned long long n_above = 0, m_above = 0;
+  GSel res{};
+  for (int shift = W - 8; shift >= 0; shift -= 8) {
+    for (int i = tid; i < kHCopies * 256; i += kGThreads) {
+      (&hist->cnt[0][0])[i] = 0;
+      (&hist->mass[0][0])[i] = 0;
+    }
+    __syncthreads();
+    const bool top = shift + 8 >= W;
+    g_for_row<ES>(row, V, [&](int32_t, float x) {
+      const uint32_t k = gkey<ES>(x);
+      if (top || (k >> (shift + 8)) == prefix) {
+        const uint32_t d = (k >> shift) & 255u;
+        atomicAdd(&hist->cnt[copy][d], 1u);
+        atomicAdd(&hist->mass[copy][d], gweight(x, sc, h));
+      }
+    });
+    __syncthreads();
+    if (warp == 0) {  // lane l holds bins 255 - 8 l .. 248 - 8 l, highest first
+      auto bin_n = [&](int b) {
+        unsigned long long n = 0;
+#pragma unroll
+        for (int c = 0; c < kHCopies; ++c) n += hist->cnt[c][b];
+        return n;
+      };
+      auto bin_m = [&](int b) {
+        unsigned long long m = 0;
+#pragma unroll
+        for (int c = 0; c < kHCopies; ++c) m += hist->mass[c][b];
+        return m;
+      };
+      unsigned long long ln = 0, lm = 0;
+      for (int j = 0; j < 8; ++j) {
+        ln += bin_n(255 - 8 * lane - j);
+        lm += bin_m(255 - 8 * lane - j);
+      }
+      unsigned long long in = ln, im = lm;  // inclusive scans over lanes
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const unsigned long long yn = __shfl_up_sync(0xffffffffu, in, off);
+        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, off);
+        if (lane >= off) {
+          in += yn;
+          im += ym;
+        }
+      }
+      const unsigned long long need = target - (by_mass ? m_above : n_above);
+      const bool reach = (by_mass ? im : in) >= need;
+      const unsigned rl = __ballot_sync(0xffffffffu, reach);
+      const int L = rl ? __ffs(rl) - 1 : 31;  // the target is within the row's total
+      if (lane == L) {
+        unsigned long long an = in - ln, am = im - lm;  // bins of earlier lanes
+        int bin = 255 - 8 * lane - 7;
+        unsigned long long tn = 0, tm = 0;
+        for (int j = 0; j < 8; ++j) {
+          const int b = 255 - 8 * lane - j;
+          tn = bin_n(b);
+          tm = bin_m(b);
+          bin = b;
+          if ((by_mass ? am + tm : an + tn) >= need) break;
+          an += tn;
+          am += tm;
+        }
+        red[0] = static_cast<unsigned long long>(bin);
+        red[1] = an;
+        red[2] = am;
+        red[3] = tn;
+        red[4] = tm;
+      }
+    }
+    __syncthreads();
+    prefix = (prefix << 8) | static_cast<uint32_t>(red[0]);
+    n_above += red[1];
+    m_above += red[2];
+    res.ties = red[3];
+    res.m_ties = red[4];
+    __syncthreads();
+  }
+  res.t = prefix;
+  res.n_above = n_above;
+  res.m_above = m_above;
+  return res;
+}
+
 // Kept set and statistics of one row (all threads of the CTA).
 template <int ES>
 __device__ __forceinline__ GRow g_select_row(const Params& P, const unsigned char* row,
-                                             unsigned long long* red, int32_t* sid) {
-  constexpr int W = ES == 2 ? 16 : 32;  // key bits
+                                             unsigned long long* red, int32_t* sid, GHist* hist) {
   const int32_t V = P.V;
   const float sc = P.sc;
   GRow g{};
@@ -250,84 +365,59 @@ __device__ __forceinline__ GRow g_select_row(const Params& P, const unsigned cha
     return g;
   }
   const float h = g.h;
-  // count / fixed-point mass of the elements with key >= t (or > t)
-  auto count_ge = [&](uint32_t t) {
-    unsigned long long n = 0;
-    g_for_row<ES>(row, V, [&](int32_t, float x) { n += gkey<ES>(x) >= t; });
-    return g_sum_u64(n, red);
-  };
-  auto mass_ge = [&](uint32_t t) {
-    unsigned long long m = 0;
-    g_for_row<ES>(row, V, [&](int32_t, float x) {
-      if (gkey<ES>(x) >= t) m += gweight(x, sc, h);
-    });
-    return g_sum_u64(m, red);
-  };
-  // above t: count, mass, and the weight of value t (equal for every tie)
-  struct Above {
-    unsigned long long n, m, wt, ties;
-  };
-  auto above = [&](uint32_t t) {
-    unsigned long long n = 0, m = 0, wt = 0, ties = 0;
-    g_for_row<ES>(row, V, [&](int32_t, float x) {
-      const uint32_t k = gkey<ES>(x);
-      if (k > t) {
-        ++n;
-        m += gweight(x, sc, h);
-      } else if (k == t) {
-        ++ties;
-        wt = gweight(x, sc, h);
-      }
-    });
-    Above r;
-    r.n = g_sum_u64(n, red);
-    r.m = g_sum_u64(m, red);
-    r.ties = g_sum_u64(ties, red);
-    r.wt = g_max_u64(wt, red);
-    return r;
-  };
-
   const bool use_k = P.top_k > 0 && P.top_k < V;
   const bool use_p = P.top_p < 1.f;
-  // ---- top-k: the k-th largest value key, then its tie class
-  uint32_t tk = 0;
-  unsigned long long zk = 0, ck = 0;
-  Above ak{};
+  unsigned long long zk = 0;
+  // ---- top-k: the k-th largest value key by bisection (counting passes, no
+  //      weights), then the kept mass and the place in the tie class
   if (use_k) {
+    constexpr int W = ES == 2 ? 16 : 32;
     const unsigned long long k = static_cast<unsigned long long>(P.top_k);
+    uint32_t tk = 0;
     for (int bit = W - 1; bit >= 0; --bit) {
       const uint32_t cand = tk | (1u << bit);
-      if (count_ge(cand) >= k) tk = cand;
+      unsigned long long n = 0;
+      g_for_row<ES>(row, V, [&](int32_t, float x) { n += gkey<ES>(x) >= cand; });
+      if (g_sum_u64(n, red) >= k) tk = cand;
     }
-    ak = above(tk);
-    ck = k - ak.n;  // 1 <= ck <= ties
-    zk = ak.m + ck * ak.wt;
+    unsigned long long n = 0, m = 0, wt = 0;
+    g_for_row<ES>(row, V, [&](int32_t, float x) {
+      const uint32_t kx = gkey<ES>(x);
+      if (kx > tk) {
+        ++n;
+        m += gweight(x, P.sc, h);
+      } else if (kx == tk) {
+        wt = gweight(x, P.sc, h);  // every tie weighs the same
+      }
+    });
+    n = g_sum_u64(n, red);
+    m = g_sum_u64(m, red);
+    wt = g_max_u64(wt, red);
+    const unsigned long long ck = k - n;  // 1 <= ck <= ties
+    zk = m + ck * wt;
     g.thr_key = tk;
     g.thr_id = g_tie_id<ES>(row, V, tk, ck, red, sid);
-    g.n_kept = static_cast<int32_t>(ak.n + ck);
-  } else {
-    zk = mass_ge(0);  // every token
+    g.n_kept = static_cast<int32_t>(n + ck);
+  } else {  // every token
+    unsigned long long m = 0;
+    g_for_row<ES>(row, V, [&](int32_t, float x) { m += gweight(x, P.sc, h); });
+    zk = g_sum_u64(m, red);
   }
-  // ---- top-p over the top-k set: the shortest prefix whose mass reaches
-  //      top_p * zk (integers: the first prefix with mass >= ceil(top_p * zk))
+  // ---- top-p: the shortest prefix of the order whose mass reaches top_p *
+  //      zk (integers: the first prefix with mass >= ceil(top_p * zk)); the
+  //      top-k set is itself a prefix of the order holding zk >= that, so the
+  //      search runs over the whole row and stops inside it
   if (use_p) {
-    const unsigned long long target =
-        static_cast<unsigned long long>(ceil(static_cast<double>(P.top_p) * static_cast<double>(zk)));
-    uint32_t tp = 0;
-    for (int bit = W - 1; bit >= 0; --bit) {
-      const uint32_t cand = tp | (1u << bit);
-      const unsigned long long m = (use_k && cand <= tk) ? zk : mass_ge(cand);
-      if (m >= target) tp = cand;
-    }
-    Above ap = (use_k && tp == tk) ? ak : above(tp);
-    // mass strictly above tp inside the top-k set; tie weight of tp
-    const unsigned long long ties = (use_k && tp == tk) ? ck : ap.ties;
-    unsigned long long cp = ap.wt > 0 ? (target - ap.m + ap.wt - 1) / ap.wt : ties;
-    cp = max(1ull, min(cp, ties));
-    g.thr_key = tp;
-    g.thr_id = g_tie_id<ES>(row, V, tp, cp, red, sid);
-    g.n_kept = static_cast<int32_t>(ap.n + cp);
-    zk = ap.m + cp * ap.wt;
+    const unsigned long long target = max(1ull, static_cast<unsigned long long>(
+        ceil(static_cast<double>(P.top_p) * static_cast<double>(zk))));
+    const GSel sp = g_radix_select<ES>(row, V, P.sc, h, target, true, hist, red);
+    const unsigned long long wt = sp.ties ? sp.m_ties / sp.ties : 0;
+    unsigned long long cp = wt > 0 ? (target - sp.m_above + wt - 1) / wt : sp.ties;
+    cp = max(1ull, min(cp, sp.ties));
+    g.thr_key = sp.t;
+    g.thr_id = g_tie_id<ES>(row, V, sp.t, cp, red, sid);
+    g.n_kept = static_cast<int32_t>(sp.n_above + cp);
+    zk = sp.m_above + cp * wt;
   }
   g.z = static_cast<float>(static_cast<double>(zk) / static_cast<double>(kGFix));
   return g;
@@ -340,9 +430,10 @@ __device__ __forceinline__ float g_p(const GRow& g, float x, int32_t id, float s
 }
 
 template <int ES>
-__global__ void __launch_bounds__(kGThreads) gfilter_rows_kernel(const Params P) {
+__global__ void __launch_bounds__(kGThreads, 2) gfilter_rows_kernel(const Params P) {
   __shared__ unsigned long long red[kGWarps];
   __shared__ int32_t sid;
+  __shared__ GHist hist;
   grid_dep_launch_dependents();
   auto slot = [&](int32_t i) {  // row i's record, at FiltRow stride
     return reinterpret_cast<GRow*>(reinterpret_cast<FiltRow*>(P.filt) + i);
@@ -359,13 +450,13 @@ __global__ void __launch_bounds__(kGThreads) gfilter_rows_kernel(const Params P)
     const int32_t gd = g - r;
     const bool pair = off <= g && g < off1 - 1 && gd >= 0 && gd < P.Nd;
     const unsigned char* trow = P.tgt + static_cast<size_t>(g) * P.V * ES;
-    const GRow gt = g_select_row<ES>(P, trow, red, &sid);
+    const GRow gt = g_select_row<ES>(P, trow, red, &sid, &hist);
     GRow gdr{};
     int fl = gt.flags;
     int acc = 0;
     if (pair) {
       const unsigned char* drow = P.drf + static_cast<size_t>(gd) * P.V * ES;
-      gdr = g_select_row<ES>(P, drow, red, &sid);
+      gdr = g_select_row<ES>(P, drow, red, &sid, &hist);
       fl |= gdr.flags;
       // label: sum over both kept sets of min(p_t, p_d), element by element
       float part = 0.f;
