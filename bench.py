@@ -387,43 +387,61 @@ def run_ours(args, world, rank, local):
 
 def run_e2e(L, w, spec, mode, dev, stream, kw, K, world):
     """Same metric through the public call with host buffers: every step
-    copies the inputs from pinned host memory, verifies, and reads the
-    outputs back."""
+    copies its inputs from pinned host memory, verifies, and reads the
+    outputs back.  As in a serving loop, the upload of the next step's inputs
+    (on a copy stream, into the other of two device input sets) overlaps the
+    current step's verify; each step still waits for its own upload."""
     host = {n: getattr(w, n).cpu().pin_memory() for n in
             ("target", "draft", "draft_tokens", "uniforms", "verify_lens", "row_offsets")}
-    devbuf = {n: torch.empty_like(t, device=dev) for n, t in host.items()}
+    devbufs = [{n: torch.empty_like(t, device=dev) for n, t in host.items()} for _ in range(2)]
     out = kw["out"]
     h_out = [torch.empty(out.tokens.shape, dtype=torch.int32).pin_memory(),
              torch.empty(out.accept_len.shape, dtype=torch.int32).pin_memory(),
              torch.empty(out.conf.shape, dtype=torch.float32).pin_memory()]
-    call = L.prepare("spec_verify", devbuf["target"], devbuf["draft"], devbuf["draft_tokens"],
-                     devbuf["uniforms"], devbuf["verify_lens"], devbuf["row_offsets"], **kw)
+    calls = [L.prepare("spec_verify", d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                       d["verify_lens"], d["row_offsets"], **kw) for d in devbufs]
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out)
     steps = max(3, min(K, 30))
+    copy_stream = torch.cuda.Stream(dev)
+    done = [torch.cuda.Event(), torch.cuda.Event()]  # verify of the set finished reading it
+    for e in done:
+        e.record(stream)
 
-    def step():
-        for n in host:
-            devbuf[n].copy_(host[n], non_blocking=True)
-        call()
-        h_out[0].copy_(out.tokens, non_blocking=True)
-        h_out[1].copy_(out.accept_len, non_blocking=True)
-        h_out[2].copy_(out.conf, non_blocking=True)
+    def upload(i):
+        copy_stream.wait_event(done[i % 2])  # the set is free again
+        with torch.cuda.stream(copy_stream):
+            for n in host:
+                devbufs[i % 2][n].copy_(host[n], non_blocking=True)
+        ev = torch.cuda.Event()
+        ev.record(copy_stream)
+        return ev
 
-    for _ in range(2):
-        step()
+    def run(n_steps):
+        ready = upload(0)
+        for i in range(n_steps):
+            stream.wait_event(ready)
+            nxt = upload(i + 1) if i + 1 < n_steps else None
+            calls[i % 2]()
+            done[i % 2].record(stream)
+            h_out[0].copy_(out.tokens, non_blocking=True)
+            h_out[1].copy_(out.accept_len, non_blocking=True)
+            h_out[2].copy_(out.conf, non_blocking=True)
+            ready = nxt
+
+    run(2)
     torch.cuda.synchronize(dev)
     barrier(world)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
-        step()
+    copy_stream.wait_stream(stream)  # the first upload starts inside the timed region
+    run(steps)
     b.record(stream)
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
     value = sum_over_ranks(steps * w.n_draft_rows, world, dev) / (ms / 1e3)
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps}
+            "steps": steps, "overlap": "next step's upload during this step's verify"}
 
 
 def run_schedule(args, rank):
