@@ -10,16 +10,18 @@
 // t and an id, the set being the tokens above t plus the tokens at t up to
 // that id.
 //
-// The top-k threshold is found by bisection over the value key (16 bits for
-// bf16, 32 for fp32), one counting pass per probe; the top-p threshold by a
-// radix select, one pass per 8-bit digit: a histogram of counts and of
-// weights w = exp2(x sc - h) (h = x_max sc) over the elements that match the
-// digits chosen so far, then the bin where the cumulative mass from the top
-// reaches the target.  Weights are summed as
-// fixed-point integers of 2^-40, so every sum is exact and the same in any
-// order.  Inside the tie class of the final value, the cut falls after c
-// tokens of equal weight, c from integer arithmetic; a counting pass finds
-// the id of the c-th.
+// Both thresholds come from one search scheme along that order, exact and
+// independent of the visiting order.  Weights w = exp2(x sc - h) (h = x_max
+// sc) are summed as fixed-point integers of 2^-40.  Level 1 is one pass: a
+// histogram of masses (and, for top-k, counts) over weight bins, eighths of
+// a binade of w, which are runs of the order and spread a row's tokens
+// thinly (few lanes of a warp meet on one bin).  The bin where the
+// cumulative count reaches k, or the cumulative mass reaches
+// ceil(top_p * kept mass), is then searched by the key's 8-bit digits (two
+// passes for bf16, four for fp32) over that bin's tokens only, with
+// warp-aggregated updates.  Inside the tie class of the final value every
+// token weighs the same, so the cut falls after c of them, c from integer
+// arithmetic; a counting pass finds the id of the c-th.
 //
 //  gfilter_rows_kernel      one CTA per target row: the kept sets of the row
 //                           and of its draft partner, the label
@@ -43,6 +45,10 @@ namespace sv {
 constexpr int kGThreads = 512;
 constexpr int kGWarps = kGThreads / 32;
 constexpr float kGFix = 1099511627776.f;  // 2^40: weight units of the exact sums
+constexpr int kGUnroll = 4;    // 16-byte vectors in flight per thread in a row pass
+constexpr int kGBins = 512;    // level-1 bins: eighths of a binade of the weight
+constexpr int kL1Copies = 4;   // level-1 histogram copies
+constexpr int kDCopies = 2;    // key-digit histogram copies
 
 // A row's kept set and statistics (stored in the row's FiltRow slot of the
 // workspace).
@@ -118,60 +124,186 @@ __device__ __forceinline__ float g_sum_f32(float v, float* red) {
   return t;
 }
 
-// Visit every element (id, logit) of a row of V logits: thread t takes the
-// 16-byte vectors t, t + NT, ... of the row's aligned cover.
-template <int ES, typename F>
-__device__ __forceinline__ void g_for_row(const unsigned char* row, int32_t V, F&& f) {
+// The 16-byte aligned cover of a row: its first vector, the elements of the
+// cover before the row, and the number of vectors.
+struct GCover {
+  const unsigned char* base;
+  int32_t hoff;
+  int32_t nvec;
+};
+
+template <int ES>
+__device__ __forceinline__ GCover g_cover(const unsigned char* row, int32_t V) {
   constexpr int VEC = 16 / ES;
   const uintptr_t gs = reinterpret_cast<uintptr_t>(row);
   const uintptr_t as = gs & ~static_cast<uintptr_t>(15);
-  const int32_t hoff = static_cast<int32_t>((gs - as) / ES);
-  const int32_t nvec = (hoff + V + VEC - 1) / VEC;
-  const unsigned char* base = reinterpret_cast<const unsigned char*>(as);
-  for (int32_t k = threadIdx.x; k < nvec; k += kGThreads) {
-    float x[VEC];
-    load_vec_raw<ES>(base, k, x);  // 16 bytes of the cover (inside the allocation's 16-byte blocks)
+  GCover c;
+  c.base = reinterpret_cast<const unsigned char*>(as);
+  c.hoff = static_cast<int32_t>((gs - as) / ES);
+  c.nvec = (c.hoff + V + VEC - 1) / VEC;
+  return c;
+}
+
+// 16 bytes of a cover (inside the allocation's 16-byte blocks), read-only path.
+__device__ __forceinline__ uint4 g_ld16(const unsigned char* base, int32_t k) {
+  return __ldg(reinterpret_cast<const uint4*>(base) + k);
+}
+
+template <int ES>
+__device__ __forceinline__ void g_unpack(const uint4& w, float* x) {
+  if (ES == 2) {
+    x[0] = bf16lo(w.x); x[1] = bf16hi(w.x); x[2] = bf16lo(w.y); x[3] = bf16hi(w.y);
+    x[4] = bf16lo(w.z); x[5] = bf16hi(w.z); x[6] = bf16lo(w.w); x[7] = bf16hi(w.w);
+  } else {
+    x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+  }
+}
+
+// Visit every element of a row of V logits.  Warp w takes the vectors
+// 32 w + lane + 512 i of the row's cover, kGUnroll of them loaded before the
+// first is used; f(id, x, ok) is called by the 32 lanes of a warp together,
+// ok false for cover elements outside the row.  A thread meets its ids in
+// ascending order.
+template <int ES, typename F>
+__device__ __forceinline__ void g_for_row(const unsigned char* row, int32_t V, F&& f) {
+  constexpr int VEC = 16 / ES;
+  const GCover c = g_cover<ES>(row, V);
+  const int lane = threadIdx.x & 31;
+  for (int32_t k0 = threadIdx.x - lane; k0 < c.nvec; k0 += kGUnroll * kGThreads) {
+    uint4 w[kGUnroll];
 #pragma unroll
-    for (int l = 0; l < VEC; ++l) {
-      const int32_t id = k * VEC - hoff + l;
-      if (id >= 0 && id < V) f(id, x[l]);
+    for (int u = 0; u < kGUnroll; ++u) {
+      const int32_t k = k0 + u * kGThreads + lane;
+      w[u] = k < c.nvec ? g_ld16(c.base, k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kGUnroll; ++u) {
+      const int32_t k = k0 + u * kGThreads + lane;
+      float x[VEC];
+      g_unpack<ES>(w[u], x);
+#pragma unroll
+      for (int l = 0; l < VEC; ++l) {
+        const int32_t id = k * VEC - c.hoff + l;
+        f(id, x[l], k < c.nvec && id >= 0 && id < V);
+      }
     }
   }
 }
 
-// The c-th smallest id (c >= 1) among the elements with key == t: warps
-// count the ties of contiguous ranges of the row, the warp whose range holds
-// the c-th walks it 32 vectors a step.
+// Visit every id of two rows of V logits together: f(id, a_id, b_id).  Rows
+// with the same 16-byte phase go by vectors, two of each row in flight per
+// thread; others element by element.
+template <int ES, typename F>
+__device__ __forceinline__ void g_for_pair(const unsigned char* a, const unsigned char* b,
+                                           int32_t V, F&& f) {
+  constexpr int VEC = 16 / ES;
+  const GCover ca = g_cover<ES>(a, V), cb = g_cover<ES>(b, V);
+  if (ca.hoff != cb.hoff) {
+    for (int32_t v = threadIdx.x; v < V; v += kGThreads) f(v, load_elem<ES>(a, v), load_elem<ES>(b, v));
+    return;
+  }
+  for (int32_t k0 = threadIdx.x; k0 < ca.nvec; k0 += 2 * kGThreads) {
+    uint4 wa[2], wb[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int32_t k = k0 + u * kGThreads;
+      if (k < ca.nvec) {
+        wa[u] = g_ld16(ca.base, k);
+        wb[u] = g_ld16(cb.base, k);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int32_t k = k0 + u * kGThreads;
+      if (k < ca.nvec) {
+        float xa[VEC], xb[VEC];
+        g_unpack<ES>(wa[u], xa);
+        g_unpack<ES>(wb[u], xb);
+#pragma unroll
+        for (int l = 0; l < VEC; ++l) {
+          const int32_t id = k * VEC - ca.hoff + l;
+          if (id >= 0 && id < V) f(id, xa[l], xb[l]);
+        }
+      }
+    }
+  }
+}
+
+// The logit whose value key is t (gkey inverted).
 template <int ES>
-__device__ __forceinline__ int32_t g_tie_id(const unsigned char* row, int32_t V, uint32_t t,
-                                            unsigned long long c, unsigned long long* red,
-                                            int32_t* shared_id) {
+__device__ __forceinline__ float gkey_value(uint32_t t) {
+  const uint32_t k = ES == 2 ? t << 16 : t;
+  const uint32_t u = (k & 0x80000000u) ? (k & 0x7fffffffu) : ~k;
+  return __uint_as_float(ES == 2 ? (u & 0xffff0000u) : u);
+}
+
+// Level-1 bin of a logit from its log2 weight y = x sc - h (about 0 at the
+// row maximum, below it elsewhere): floor(-8 y) clamped to [0, kGBins - 1],
+// eighths of a binade of the weight.  It never falls along the (value desc,
+// id asc) order, so each bin holds a run of that order (equal values share
+// a bin); weights in the last bin are below 2^-63, 0 in fixed point.
+__device__ __forceinline__ int gbin(float y) {
+  return min(kGBins - 1, __float2int_rz(fmaxf(-8.f * y, 0.f)));
+}
+
+// The c-th smallest id (c >= 1) among the elements with key == t, and the
+// number of elements with key > t: warps count over contiguous ranges of the
+// row (kGUnroll vectors a lane in flight), the warp whose range holds the
+// c-th walks it 32 vectors a step.
+struct GTie {
+  int32_t id;
+  unsigned long long n_above;
+};
+
+template <int ES>
+__device__ __forceinline__ GTie g_tie_id(const unsigned char* row, int32_t V, uint32_t t,
+                                         unsigned long long c, unsigned long long* red,
+                                         int32_t* shared_id) {
   constexpr int VEC = 16 / ES;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const uintptr_t gs = reinterpret_cast<uintptr_t>(row);
-  const uintptr_t as = gs & ~static_cast<uintptr_t>(15);
-  const int32_t hoff = static_cast<int32_t>((gs - as) / ES);
-  const int32_t nvec = (hoff + V + VEC - 1) / VEC;
-  const unsigned char* base = reinterpret_cast<const unsigned char*>(as);
-  const int32_t per = (nvec + kGWarps - 1) / kGWarps;  // vectors per warp range
-  const int32_t k0 = min(nvec, warp * per), k1 = min(nvec, k0 + per);
-  auto ties = [&](int32_t k) {  // ties in vector k, and their ids in order
+  const GCover cv = g_cover<ES>(row, V);
+  const int32_t per = (cv.nvec + kGWarps - 1) / kGWarps;  // vectors per warp range
+  const int32_t k0 = min(cv.nvec, warp * per), k1 = min(cv.nvec, k0 + per);
+  auto scan = [&](const uint4& w, int32_t k, unsigned& above) {  // tie mask, count above
     float x[VEC];
-    load_vec_raw<ES>(base, k, x);
+    g_unpack<ES>(w, x);
     unsigned m = 0;
 #pragma unroll
     for (int l = 0; l < VEC; ++l) {
-      const int32_t id = k * VEC - hoff + l;
-      if (id >= 0 && id < V && gkey<ES>(x[l]) == t) m |= 1u << l;
+      const int32_t id = k * VEC - cv.hoff + l;
+      const uint32_t kx = gkey<ES>(x[l]);
+      if (id >= 0 && id < V) {
+        if (kx == t) m |= 1u << l;
+        above += kx > t;
+      }
     }
     return m;
   };
-  unsigned long long n = 0;
-  for (int32_t k = k0 + lane; k < k1; k += 32) n += __popc(ties(k));
+  unsigned long long n = 0, na = 0;
+  for (int32_t kb = k0; kb < k1; kb += 32 * kGUnroll) {
+    uint4 w[kGUnroll];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
+    for (int u = 0; u < kGUnroll; ++u) {
+      const int32_t k = kb + 32 * u + lane;
+      w[u] = k < k1 ? g_ld16(cv.base, k) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kGUnroll; ++u) {
+      const int32_t k = kb + 32 * u + lane;
+      if (k < k1) {
+        unsigned a = 0;
+        n += __popc(scan(w[u], k, a));
+        na += a;
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    n += __shfl_xor_sync(0xffffffffu, n, off);
+    na += __shfl_xor_sync(0xffffffffu, na, off);
+  }
   if (lane == 0) red[warp] = n;
-  if (threadIdx.x == 0) *shared_id = -1;
   __syncthreads();
   unsigned long long before = 0;
   int owner = -1;
@@ -180,11 +312,18 @@ __device__ __forceinline__ int32_t g_tie_id(const unsigned char* row, int32_t V,
     if (owner < 0) before += red[w];
   }
   __syncthreads();
+  if (lane == 0) red[warp] = na;
+  if (threadIdx.x == 0) *shared_id = -1;
+  __syncthreads();
+  GTie res;
+  res.n_above = 0;
+  for (int w = 0; w < kGWarps; ++w) res.n_above += red[w];
   if (warp == owner) {
     unsigned long long left = c - before;  // >= 1
     for (int32_t kb = k0; kb < k1; kb += 32) {
       const int32_t k = kb + lane;
-      const unsigned m = k < k1 ? ties(k) : 0u;
+      unsigned a = 0;
+      const unsigned m = k < k1 ? scan(g_ld16(cv.base, k), k, a) : 0u;
       unsigned cnt = __popc(m), incl = cnt;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -197,7 +336,7 @@ __device__ __forceinline__ int32_t g_tie_id(const unsigned char* row, int32_t V,
           unsigned r = static_cast<unsigned>(left - (incl - cnt));  // r-th tie of this vector
           unsigned mm = m;
           for (unsigned i = 1; i < r; ++i) mm &= mm - 1;
-          *shared_id = k * VEC - hoff + (__ffs(mm) - 1);
+          *shared_id = k * VEC - cv.hoff + (__ffs(mm) - 1);
         }
         break;
       }
@@ -205,122 +344,148 @@ __device__ __forceinline__ int32_t g_tie_id(const unsigned char* row, int32_t V,
     }
   }
   __syncthreads();
-  const int32_t id = *shared_id;
+  res.id = *shared_id;
   __syncthreads();
-  return id;
+  return res;
 }
 
-constexpr int kHCopies = 8;  // histogram copies (two warps share one)
-
-// Shared histograms of one radix level: per copy 256 bins of a count and a
-// fixed-point mass.
+// Shared histograms of counts and fixed-point masses: level 1 (kGBins weight
+// bins; kGWarps / kL1Copies warps share a copy) and the key-digit levels (256
+// bins).
 struct GHist {
-  uint32_t cnt[kHCopies][256];
-  unsigned long long mass[kHCopies][256];
+  unsigned long long l1m[kL1Copies][kGBins];
+  uint32_t l1n[kL1Copies][kGBins];
+  unsigned long long dm[kDCopies][256];
+  uint32_t dn[kDCopies][256];
 };
 
-// The value key t of the first element, in (value desc, id asc) order, at
-// which the cumulative count (by_mass false) or fixed-point mass reaches
-// `target` (>= 1, at most the row's total), with the count and mass of the
-// keys above t and the count and total weight of the keys equal to t (the
-// top-p search; top-k counts by bisection, which needs no weights).  One
-// pass per 8-bit digit of the key (two for bf16, four for fp32): a histogram
-// of the elements that match the digits chosen so far, then the bin where
-// the target falls.
+// Warp-aggregated histogram update: every lane with d >= 0 adds one to count
+// bin d and w to mass bin d, the lanes of a warp that share a bin with one
+// atomic per bin.  All 32 lanes of the warp call it.
+__device__ __forceinline__ void g_add_agg(uint32_t* n, unsigned long long* m, int d,
+                                          unsigned long long w) {
+  const int lane = threadIdx.x & 31;
+  unsigned todo = __ballot_sync(0xffffffffu, d >= 0);
+  while (todo) {
+    const int src = __ffs(todo) - 1;
+    const int ds = __shfl_sync(0xffffffffu, d, src);
+    const bool mine = d == ds;
+    const unsigned grp = __ballot_sync(0xffffffffu, mine);
+    unsigned long long s = mine ? w : 0ull;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == src) {
+      atomicAdd(n + ds, static_cast<uint32_t>(__popc(grp)));
+      if (s) atomicAdd(m + ds, s);
+    }
+    todo &= ~grp;
+  }
+}
+
+// Warp 0 only: over NB bins in order (j = 0 first along the value-desc
+// order; bin_n / bin_m give a bin's count and mass), the first bin at which
+// the cumulative count (by_mass false) or mass reaches need.  Writes the bin,
+// the count and the mass of the bins before it and the bin's count to
+// out[0..3].
+template <int NB, typename FN, typename FM>
+__device__ __forceinline__ void g_find(FN&& bin_n, FM&& bin_m, bool by_mass,
+                                       unsigned long long need, unsigned long long* out) {
+  constexpr int PER = NB / 32;
+  const int lane = threadIdx.x & 31;
+  unsigned long long ln = 0, lm = 0;
+  for (int i = 0; i < PER; ++i) {
+    ln += bin_n(lane * PER + i);
+    lm += bin_m(lane * PER + i);
+  }
+  unsigned long long in = ln, im = lm;  // inclusive scans over lanes
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const unsigned long long yn = __shfl_up_sync(0xffffffffu, in, off);
+    const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, off);
+    if (lane >= off) {
+      in += yn;
+      im += ym;
+    }
+  }
+  const unsigned rl = __ballot_sync(0xffffffffu, (by_mass ? im : in) >= need);
+  const int L = rl ? __ffs(rl) - 1 : 31;  // need is within the total
+  if (lane == L) {
+    unsigned long long an = in - ln, am = im - lm;  // bins of earlier lanes
+    for (int i = 0; i < PER; ++i) {
+      const int j = L * PER + i;
+      const unsigned long long cn = bin_n(j), cm = bin_m(j);
+      if ((by_mass ? am + cm : an + cn) >= need || i == PER - 1) {
+        out[0] = static_cast<unsigned long long>(j);
+        out[1] = an;
+        out[2] = am;
+        out[3] = cn;
+        break;
+      }
+      an += cn;
+      am += cm;
+    }
+  }
+}
+
+// Search along the (value desc, id asc) order inside level-1 bin b: the value
+// key t of the element at which the cumulative count (by_mass false) or mass
+// of the bin's elements reaches need (>= 1, at most the bin's total), the
+// count and mass of the bin's keys above t, and the count of keys equal to t.
+// One pass per 8-bit digit of the key (two for bf16, four for fp32), each a
+// histogram of the bin's elements matching the digits chosen so far.
 struct GSel {
   uint32_t t;
-  unsigned long long n_above, m_above, ties, m_ties;
+  unsigned long long n_above, m_above, ties;
 };
 
 template <int ES>
-__device__ __forceinline__ GSel g_radix_select(const unsigned char* row, int32_t V, float sc, float h,
-                                               unsigned long long target, bool by_mass,
-                                               GHist* hist, unsigned long long* red) {
+__device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, float sc, float h,
+                                         int b, unsigned long long need, bool by_mass,
+                                         GHist* hist, unsigned long long* red) {
   constexpr int W = ES == 2 ? 16 : 32;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int copy = warp % kHCopies;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int cd = warp % kDCopies;
   uint32_t prefix = 0;
-  unsigned long long n_above = 0, m_above = 0;
   GSel res{};
   for (int shift = W - 8; shift >= 0; shift -= 8) {
-    for (int i = tid; i < kHCopies * 256; i += kGThreads) {
-      (&hist->cnt[0][0])[i] = 0;
-      (&hist->mass[0][0])[i] = 0;
+    for (int i = tid; i < kDCopies * 256; i += kGThreads) {
+      (&hist->dn[0][0])[i] = 0;
+      (&hist->dm[0][0])[i] = 0;
     }
     __syncthreads();
-    const bool top = shift + 8 >= W;
-    g_for_row<ES>(row, V, [&](int32_t, float x) {
+    g_for_row<ES>(row, V, [&](int32_t, float x, bool ok) {
+      const float y = fmaf(x, sc, -h);
       const uint32_t k = gkey<ES>(x);
-      if (top || (k >> (shift + 8)) == prefix) {
-        const uint32_t d = (k >> shift) & 255u;
-        atomicAdd(&hist->cnt[copy][d], 1u);
-        atomicAdd(&hist->mass[copy][d], gweight(x, sc, h));
-      }
+      const bool in = ok && gbin(y) == b && (k >> shift >> 8) == prefix;
+      const unsigned long long w = in ? __float2ull_rn(ex2(y) * kGFix) : 0ull;
+      g_add_agg(hist->dn[cd], hist->dm[cd], in ? static_cast<int>((k >> shift) & 255u) : -1, w);
     });
     __syncthreads();
-    if (warp == 0) {  // lane l holds bins 255 - 8 l .. 248 - 8 l, highest first
-      auto bin_n = [&](int b) {
-        unsigned long long n = 0;
+    if (warp == 0) {
+      g_find<256>(
+          [&](int j) {
+            unsigned long long s = 0;
 #pragma unroll
-        for (int c = 0; c < kHCopies; ++c) n += hist->cnt[c][b];
-        return n;
-      };
-      auto bin_m = [&](int b) {
-        unsigned long long m = 0;
+            for (int c = 0; c < kDCopies; ++c) s += hist->dn[c][255 - j];
+            return s;
+          },
+          [&](int j) {
+            unsigned long long s = 0;
 #pragma unroll
-        for (int c = 0; c < kHCopies; ++c) m += hist->mass[c][b];
-        return m;
-      };
-      unsigned long long ln = 0, lm = 0;
-      for (int j = 0; j < 8; ++j) {
-        ln += bin_n(255 - 8 * lane - j);
-        lm += bin_m(255 - 8 * lane - j);
-      }
-      unsigned long long in = ln, im = lm;  // inclusive scans over lanes
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const unsigned long long yn = __shfl_up_sync(0xffffffffu, in, off);
-        const unsigned long long ym = __shfl_up_sync(0xffffffffu, im, off);
-        if (lane >= off) {
-          in += yn;
-          im += ym;
-        }
-      }
-      const unsigned long long need = target - (by_mass ? m_above : n_above);
-      const bool reach = (by_mass ? im : in) >= need;
-      const unsigned rl = __ballot_sync(0xffffffffu, reach);
-      const int L = rl ? __ffs(rl) - 1 : 31;  // the target is within the row's total
-      if (lane == L) {
-        unsigned long long an = in - ln, am = im - lm;  // bins of earlier lanes
-        int bin = 255 - 8 * lane - 7;
-        unsigned long long tn = 0, tm = 0;
-        for (int j = 0; j < 8; ++j) {
-          const int b = 255 - 8 * lane - j;
-          tn = bin_n(b);
-          tm = bin_m(b);
-          bin = b;
-          if ((by_mass ? am + tm : an + tn) >= need) break;
-          an += tn;
-          am += tm;
-        }
-        red[0] = static_cast<unsigned long long>(bin);
-        red[1] = an;
-        red[2] = am;
-        red[3] = tn;
-        red[4] = tm;
-      }
+            for (int c = 0; c < kDCopies; ++c) s += hist->dm[c][255 - j];
+            return s;
+          },
+          by_mass, need, red);
     }
     __syncthreads();
-    prefix = (prefix << 8) | static_cast<uint32_t>(red[0]);
-    n_above += red[1];
-    m_above += red[2];
+    prefix = (prefix << 8) | (255u - static_cast<uint32_t>(red[0]));
+    res.n_above += red[1];
+    res.m_above += red[2];
     res.ties = red[3];
-    res.m_ties = red[4];
+    need -= by_mass ? red[2] : red[1];
     __syncthreads();
   }
   res.t = prefix;
-  res.n_above = n_above;
-  res.m_above = m_above;
   return res;
 }
 
@@ -330,25 +495,27 @@ __device__ __forceinline__ GRow g_select_row(const Params& P, const unsigned cha
                                              unsigned long long* red, int32_t* sid, GHist* hist) {
   const int32_t V = P.V;
   const float sc = P.sc;
+  const int tid = threadIdx.x, warp = tid >> 5;
   GRow g{};
   // ---- maximum, its lowest id, non-finite inputs
   float mx = -INFINITY;
   int32_t arg = 0x7fffffff;
   bool bad = false;
-  g_for_row<ES>(row, V, [&](int32_t id, float x) {
+  g_for_row<ES>(row, V, [&](int32_t id, float x, bool ok) {
+    if (!ok) return;
     if (x != x || x == INFINITY) bad = true;
     if (x > mx) { mx = x; arg = id; }
   });
   const float xmax = warp_max_f32(mx);
   float* fred = reinterpret_cast<float*>(red);
-  if ((threadIdx.x & 31) == 0) fred[threadIdx.x >> 5] = xmax;
+  if ((tid & 31) == 0) fred[warp] = xmax;
   __syncthreads();
   float gmx = -INFINITY;
   for (int w = 0; w < kGWarps; ++w) gmx = fmaxf(gmx, fred[w]);
   __syncthreads();
   const int32_t a_w = __reduce_min_sync(0xffffffffu, mx == gmx ? arg : 0x7fffffff);
   int* ired = reinterpret_cast<int*>(red);
-  if ((threadIdx.x & 31) == 0) ired[threadIdx.x >> 5] = a_w;
+  if ((tid & 31) == 0) ired[warp] = a_w;
   __syncthreads();
   int32_t gar = 0x7fffffff;
   for (int w = 0; w < kGWarps; ++w) gar = min(gar, ired[w]);
@@ -367,57 +534,79 @@ __device__ __forceinline__ GRow g_select_row(const Params& P, const unsigned cha
   const float h = g.h;
   const bool use_k = P.top_k > 0 && P.top_k < V;
   const bool use_p = P.top_p < 1.f;
-  unsigned long long zk = 0;
-  // ---- top-k: the k-th largest value key by bisection (counting passes, no
-  //      weights), then the kept mass and the place in the tie class
-  if (use_k) {
-    constexpr int W = ES == 2 ? 16 : 32;
-    const unsigned long long k = static_cast<unsigned long long>(P.top_k);
-    uint32_t tk = 0;
-    for (int bit = W - 1; bit >= 0; --bit) {
-      const uint32_t cand = tk | (1u << bit);
-      unsigned long long n = 0;
-      g_for_row<ES>(row, V, [&](int32_t, float x) { n += gkey<ES>(x) >= cand; });
-      if (g_sum_u64(n, red) >= k) tk = cand;
-    }
-    unsigned long long n = 0, m = 0, wt = 0;
-    g_for_row<ES>(row, V, [&](int32_t, float x) {
-      const uint32_t kx = gkey<ES>(x);
-      if (kx > tk) {
-        ++n;
-        m += gweight(x, P.sc, h);
-      } else if (kx == tk) {
-        wt = gweight(x, P.sc, h);  // every tie weighs the same
-      }
-    });
-    n = g_sum_u64(n, red);
-    m = g_sum_u64(m, red);
-    wt = g_max_u64(wt, red);
-    const unsigned long long ck = k - n;  // 1 <= ck <= ties
-    zk = m + ck * wt;
-    g.thr_key = tk;
-    g.thr_id = g_tie_id<ES>(row, V, tk, ck, red, sid);
-    g.n_kept = static_cast<int32_t>(n + ck);
-  } else {  // every token
-    unsigned long long m = 0;
-    g_for_row<ES>(row, V, [&](int32_t, float x) { m += gweight(x, P.sc, h); });
-    zk = g_sum_u64(m, red);
+  // ---- level 1, one pass: masses (and, for top-k, counts) of the weight bins
+  const int c1 = warp % kL1Copies;
+  for (int i = tid; i < kL1Copies * kGBins; i += kGThreads) {
+    (&hist->l1n[0][0])[i] = 0;
+    (&hist->l1m[0][0])[i] = 0;
   }
-  // ---- top-p: the shortest prefix of the order whose mass reaches top_p *
-  //      zk (integers: the first prefix with mass >= ceil(top_p * zk)); the
-  //      top-k set is itself a prefix of the order holding zk >= that, so the
-  //      search runs over the whole row and stops inside it
+  __syncthreads();
+  g_for_row<ES>(row, V, [&](int32_t, float x, bool ok) {
+    if (!ok) return;
+    const float y = fmaf(x, sc, -h);
+    const int b = gbin(y);
+    if (use_k) atomicAdd(&hist->l1n[c1][b], 1u);
+    const unsigned long long w = __float2ull_rn(ex2(y) * kGFix);
+    if (w) atomicAdd(&hist->l1m[c1][b], w);
+  });
+  __syncthreads();
+  auto l1n = [&](int j) {
+    unsigned long long s = 0;
+#pragma unroll
+    for (int c = 0; c < kL1Copies; ++c) s += hist->l1n[c][j];
+    return s;
+  };
+  auto l1m = [&](int j) {
+    unsigned long long s = 0;
+#pragma unroll
+    for (int c = 0; c < kL1Copies; ++c) s += hist->l1m[c][j];
+    return s;
+  };
+  unsigned long long zt = 0;  // the row's total mass
+  for (int j = tid; j < kGBins; j += kGThreads) zt += l1m(j);
+  zt = g_sum_u64(zt, red);
+  unsigned long long zk = zt;  // mass of the kept set
+  if (use_k) {
+    // ---- top-k: the bin holding the k-th element by count, then its key
+    //      digits; the kept mass from the bins and digits above and the tie
+    //      weight (every tie weighs the same)
+    const unsigned long long k = static_cast<unsigned long long>(P.top_k);
+    if (warp == 0) g_find<kGBins>(l1n, l1m, false, k, red);
+    __syncthreads();
+    const int bk = static_cast<int>(red[0]);
+    const unsigned long long nb = red[1], mb = red[2];
+    __syncthreads();
+    const GSel s = g_digits<ES>(row, V, sc, h, bk, k - nb, false, hist, red);
+    const unsigned long long n_above = nb + s.n_above;
+    const unsigned long long ck = k - n_above;  // 1 <= ck <= ties
+    const unsigned long long wt = gweight(gkey_value<ES>(s.t), sc, h);
+    zk = mb + s.m_above + ck * wt;
+    g.thr_key = s.t;
+    g.n_kept = static_cast<int32_t>(n_above + ck);
+    if (!use_p) g.thr_id = g_tie_id<ES>(row, V, s.t, ck, red, sid).id;
+  }
   if (use_p) {
+    // ---- top-p: the shortest prefix of the order whose mass reaches top_p *
+    //      zk (integers: the first prefix with mass >= ceil(top_p * zk)); the
+    //      top-k set is itself a prefix of the order holding zk >= that, so the
+    //      search runs over the whole row and stops inside it
     const unsigned long long target = max(1ull, static_cast<unsigned long long>(
         ceil(static_cast<double>(P.top_p) * static_cast<double>(zk))));
-    const GSel sp = g_radix_select<ES>(row, V, P.sc, h, target, true, hist, red);
-    const unsigned long long wt = sp.ties ? sp.m_ties / sp.ties : 0;
-    unsigned long long cp = wt > 0 ? (target - sp.m_above + wt - 1) / wt : sp.ties;
-    cp = max(1ull, min(cp, sp.ties));
-    g.thr_key = sp.t;
-    g.thr_id = g_tie_id<ES>(row, V, sp.t, cp, red, sid);
-    g.n_kept = static_cast<int32_t>(sp.n_above + cp);
-    zk = sp.m_above + cp * wt;
+    if (warp == 0) g_find<kGBins>(l1n, l1m, true, target, red);
+    __syncthreads();
+    const int bp = static_cast<int>(red[0]);
+    const unsigned long long mb = red[2];
+    __syncthreads();
+    const GSel s = g_digits<ES>(row, V, sc, h, bp, target - mb, true, hist, red);
+    const unsigned long long m_above = mb + s.m_above;
+    const unsigned long long wt = gweight(gkey_value<ES>(s.t), sc, h);
+    unsigned long long cp = wt > 0 ? (target - m_above + wt - 1) / wt : s.ties;
+    cp = max(1ull, min(cp, s.ties));
+    const GTie tie = g_tie_id<ES>(row, V, s.t, cp, red, sid);
+    g.thr_key = s.t;
+    g.thr_id = tie.id;
+    g.n_kept = static_cast<int32_t>(tie.n_above + cp);
+    zk = m_above + cp * wt;
   }
   g.z = static_cast<float>(static_cast<double>(zk) / static_cast<double>(kGFix));
   return g;
@@ -461,10 +650,9 @@ __global__ void __launch_bounds__(kGThreads, 2) gfilter_rows_kernel(const Params
       // label: sum over both kept sets of min(p_t, p_d), element by element
       float part = 0.f;
       if (P.out_conf != nullptr && !fl) {
-        for (int32_t v = threadIdx.x; v < P.V; v += kGThreads) {
-          const float t = load_elem<ES>(trow, v), d = load_elem<ES>(drow, v);
+        g_for_pair<ES>(trow, drow, P.V, [&](int32_t v, float t, float d) {
           part += fminf(g_p<ES>(gt, t, v, P.sc), g_p<ES>(gdr, d, v, P.sc));
-        }
+        });
       }
       const float label = g_sum_f32(part, reinterpret_cast<float*>(red));
       const int32_t x = __ldg(P.draft_tokens + gd);
@@ -541,15 +729,42 @@ __global__ void __launch_bounds__(kGThreads) gfilter_requests_kernel(const Param
   if (residual) gd = *reinterpret_cast<const GRow*>(slots + P.Nt + off - r + a);
   const unsigned char* trow = P.tgt + static_cast<size_t>(trow_i) * P.V * ES;
   const unsigned char* drow = P.drf + static_cast<size_t>(off - r + a) * P.V * ES;
-  const int32_t E = (P.V + kGThreads - 1) / kGThreads;  // ids per thread
-  const int32_t i0 = min(P.V, tid * E), i1 = min(P.V, i0 + E);
+  // thread t owns the ids of the row cover's vectors [t EV, t EV + EV), a run
+  // of ascending ids read 16 bytes at a time
+  constexpr int VEC = 16 / ES;
+  const GCover ct = g_cover<ES>(trow, P.V), cd = g_cover<ES>(drow, P.V);
+  const bool same_phase = ct.hoff == cd.hoff;
+  const int32_t EV = (ct.nvec + kGThreads - 1) / kGThreads;
+  const int32_t k0 = min(ct.nvec, tid * EV), k1 = min(ct.nvec, k0 + EV);
+  const int32_t i0 = max(0, min(P.V, k0 * VEC - ct.hoff)), i1 = max(0, min(P.V, k1 * VEC - ct.hoff));
+  auto wfun = [&](float xt, float xd, int32_t v, bool res) {
+    const float pt = g_p<ES>(gt, xt, v, P.sc);
+    return res ? fmaxf(0.f, pt - g_p<ES>(gd, xd, v, P.sc)) : pt;
+  };
   auto weight = [&](int32_t v, bool res) {
-    const float pt = g_p<ES>(gt, load_elem<ES>(trow, v), v, P.sc);
-    return res ? fmaxf(0.f, pt - g_p<ES>(gd, load_elem<ES>(drow, v), v, P.sc)) : pt;
+    return wfun(load_elem<ES>(trow, v), res ? load_elem<ES>(drow, v) : 0.f, v, res);
   };
   for (int round = 0; round < 2; ++round) {
     float wsum = 0.f;
-    for (int32_t v = i0; v < i1; ++v) wsum += weight(v, residual);
+#pragma unroll 4
+    for (int32_t k = k0; k < k1; ++k) {
+      float xt[VEC], xd[VEC];
+      g_unpack<ES>(g_ld16(ct.base, k), xt);
+      if (residual && same_phase) {
+        g_unpack<ES>(g_ld16(cd.base, k), xd);
+      } else {
+#pragma unroll
+        for (int l = 0; l < VEC; ++l) {
+          const int32_t v = k * VEC - ct.hoff + l;
+          xd[l] = residual && v >= 0 && v < P.V ? load_elem<ES>(drow, v) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int l = 0; l < VEC; ++l) {
+        const int32_t v = k * VEC - ct.hoff + l;
+        if (v >= 0 && v < P.V) wsum += wfun(xt[l], xd[l], v, residual);
+      }
+    }
     float lo, hi, tot;
     block_scan_bounds<kGWarps>(wsum, fred, lo, hi, tot);
     if (residual && !(tot > kZeroResidual)) {  // no residual mass (rounding only): p_t
