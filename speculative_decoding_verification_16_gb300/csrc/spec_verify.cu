@@ -338,8 +338,9 @@ int run_rows(const Args& a, bool fuse) {
   cudaStream_t st = static_cast<cudaStream_t>(a.stream);
   if (P.gfilter) {  // kept sets of any size: bisection on the value key per row
     const int rows = std::max(1, std::min(a.n_target_rows, dc.sms * 2));  // 2 CTAs per SM
-    if (es == 2) return launch_plain(gfilter_rows_kernel<2>, P, rows, kGThreads, 0, dc.max_smem_optin, false, st);
-    return launch_plain(gfilter_rows_kernel<4>, P, rows, kGThreads, 0, dc.max_smem_optin, false, st);
+    constexpr int hs = static_cast<int>(sizeof(GHist));
+    if (es == 2) return launch_plain(gfilter_rows_kernel<2>, P, rows, kGThreads, hs, dc.max_smem_optin, false, st);
+    return launch_plain(gfilter_rows_kernel<4>, P, rows, kGThreads, hs, dc.max_smem_optin, false, st);
   }
   if (P.top_k > 0) {  // top-k / top-p: one streaming pass per row, no exchange
     const int rows = P.Nt + P.Nd;

@@ -45,10 +45,11 @@ namespace sv {
 constexpr int kGThreads = 512;
 constexpr int kGWarps = kGThreads / 32;
 constexpr float kGFix = 1099511627776.f;  // 2^40: weight units of the exact sums
-constexpr int kGUnroll = 4;    // 16-byte vectors in flight per thread in a row pass
+// 16-byte vectors in flight per thread in a row pass: 64 bytes, 16 logits
+template <int ES>
+__host__ __device__ constexpr int g_unroll() { return ES == 2 ? 2 : 4; }
 constexpr int kGBins = 512;    // level-1 bins: eighths of a binade of the weight
 constexpr int kL1Copies = 4;   // level-1 histogram copies
-constexpr int kDCopies = 2;    // key-digit histogram copies
 
 // A row's kept set and statistics (stored in the row's FiltRow slot of the
 // workspace).
@@ -59,7 +60,6 @@ struct GRow {
   int32_t argmax;    // lowest id holding it
   uint32_t thr_key;  // kept: key > thr_key, or key == thr_key and id <= thr_id
   int32_t thr_id;
-  int32_t n_kept;
   int32_t flags;
 };
 static_assert(sizeof(GRow) <= sizeof(FiltRow), "GRow in a FiltRow slot");
@@ -83,9 +83,27 @@ __device__ __forceinline__ bool gkept(const GRow& g, uint32_t key, int32_t id) {
   return key > g.thr_key || (key == g.thr_key && id <= g.thr_id);
 }
 
-// Fixed-point weight of logit x (exact integer units of 2^-40).
+// v * 2^40 rounded to the nearest integer (ties to even), v in [0, 2) and
+// finite, in 32-bit integer and float-add operations: at 2^23 and above the
+// product is already an integer, its 24-bit significand shifted left by the
+// exponent less 23; below, F + 2^23 lands on the grid of 1, which rounds F.
+// (A 64-bit conversion would run on the double-precision pipe.)
+__device__ __forceinline__ unsigned long long gfix(float v) {
+  const float F = v * kGFix;
+  const uint32_t b = __float_as_uint(F);
+  const unsigned long long big = static_cast<unsigned long long>((b & 0x7fffffu) | 0x800000u)
+                                 << max(0, static_cast<int>(b >> 23) - 150);
+  const uint32_t small = __float_as_uint(__fadd_rn(F, 8388608.f)) - 0x4b000000u;
+  return F < 8388608.f ? static_cast<unsigned long long>(small) : big;
+}
+
+// Fixed-point weight of a logit from its log2 weight y = x sc - h (exact
+// integer units of 2^-40).
+__device__ __forceinline__ unsigned long long gweight_y(float y) { return gfix(ex2(y)); }
+
+// Fixed-point weight of logit x.
 __device__ __forceinline__ unsigned long long gweight(float x, float sc, float h) {
-  return __float2ull_rn(ex2(fmaf(x, sc, -h)) * kGFix);
+  return gweight_y(fmaf(x, sc, -h));
 }
 
 // ---- block reductions (all threads of the CTA call them; every thread gets
@@ -168,8 +186,10 @@ __device__ __forceinline__ void g_unpack(const uint4& w, float* x) {
 template <int ES, typename F>
 __device__ __forceinline__ void g_for_row(const unsigned char* row, int32_t V, F&& f) {
   constexpr int VEC = 16 / ES;
+  constexpr int kGUnroll = g_unroll<ES>();
   const GCover c = g_cover<ES>(row, V);
   const int lane = threadIdx.x & 31;
+  const int32_t kf0 = c.hoff > 0 ? 1 : 0, kf1 = (c.hoff + V) / VEC;  // vectors inside the row
   for (int32_t k0 = threadIdx.x - lane; k0 < c.nvec; k0 += kGUnroll * kGThreads) {
     uint4 w[kGUnroll];
 #pragma unroll
@@ -177,15 +197,26 @@ __device__ __forceinline__ void g_for_row(const unsigned char* row, int32_t V, F
       const int32_t k = k0 + u * kGThreads + lane;
       w[u] = k < c.nvec ? g_ld16(c.base, k) : make_uint4(0u, 0u, 0u, 0u);
     }
+    if (k0 >= kf0 && k0 + (kGUnroll - 1) * kGThreads + 31 < kf1) {  // the warp's vectors are all inside
 #pragma unroll
-    for (int u = 0; u < kGUnroll; ++u) {
-      const int32_t k = k0 + u * kGThreads + lane;
-      float x[VEC];
-      g_unpack<ES>(w[u], x);
+      for (int u = 0; u < kGUnroll; ++u) {
+        const int32_t k = k0 + u * kGThreads + lane;
+        float x[VEC];
+        g_unpack<ES>(w[u], x);
 #pragma unroll
-      for (int l = 0; l < VEC; ++l) {
-        const int32_t id = k * VEC - c.hoff + l;
-        f(id, x[l], k < c.nvec && id >= 0 && id < V);
+        for (int l = 0; l < VEC; ++l) f(k * VEC - c.hoff + l, x[l], true);
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < kGUnroll; ++u) {
+        const int32_t k = k0 + u * kGThreads + lane;
+        float x[VEC];
+        g_unpack<ES>(w[u], x);
+#pragma unroll
+        for (int l = 0; l < VEC; ++l) {
+          const int32_t id = k * VEC - c.hoff + l;
+          f(id, x[l], k < c.nvec && id >= 0 && id < V);
+        }
       }
     }
   }
@@ -244,43 +275,43 @@ __device__ __forceinline__ float gkey_value(uint32_t t) {
 // id asc) order, so each bin holds a run of that order (equal values share
 // a bin); weights in the last bin are below 2^-63, 0 in fixed point.
 __device__ __forceinline__ int gbin(float y) {
-  return min(kGBins - 1, __float2int_rz(fmaxf(-8.f * y, 0.f)));
+  const float t = fminf(fmaxf(-8.f * y, 0.f), static_cast<float>(kGBins - 1));
+  return static_cast<int>(__float_as_uint(__fadd_rz(t, 8388608.f)) - 0x4b000000u);  // floor(t)
 }
 
-// The c-th smallest id (c >= 1) among the elements with key == t, and the
-// number of elements with key > t: warps count over contiguous ranges of the
-// row (kGUnroll vectors a lane in flight), the warp whose range holds the
-// c-th walks it 32 vectors a step.
-struct GTie {
-  int32_t id;
-  unsigned long long n_above;
-};
+// Level-1 masses are kept in 32 bits, in units of 2^gshift(b) for bin b: a
+// weight of bin b is below 2^(41 - floor(b / 8)), so w >> gshift(b) < 2^13
+// and a copy's sum over at most V / kL1Copies tokens stays below 2^32 for
+// V up to 2^21.  With the bin's count this bounds its exact mass:
+// sum(w >> s) << s <= mass < (sum(w >> s) + count) << s.
+__device__ __forceinline__ int gshift(int b) { return max(0, 28 - (b >> 3)); }
 
+// The c-th smallest id (c >= 1) among the elements with key == t: warps
+// count over contiguous ranges of the row (kGUnroll vectors a lane in
+// flight), the warp whose range holds the c-th walks it, 32 vectors a step
+// with kGUnroll steps of loads in flight.
 template <int ES>
-__device__ __forceinline__ GTie g_tie_id(const unsigned char* row, int32_t V, uint32_t t,
+__device__ __forceinline__ int32_t g_tie_id(const unsigned char* row, int32_t V, uint32_t t,
                                          unsigned long long c, unsigned long long* red,
                                          int32_t* shared_id) {
   constexpr int VEC = 16 / ES;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  constexpr int kGUnroll = g_unroll<ES>();
   const GCover cv = g_cover<ES>(row, V);
   const int32_t per = (cv.nvec + kGWarps - 1) / kGWarps;  // vectors per warp range
   const int32_t k0 = min(cv.nvec, warp * per), k1 = min(cv.nvec, k0 + per);
-  auto scan = [&](const uint4& w, int32_t k, unsigned& above) {  // tie mask, count above
+  auto scan = [&](const uint4& w, int32_t k) {  // tie mask of vector k
     float x[VEC];
     g_unpack<ES>(w, x);
     unsigned m = 0;
 #pragma unroll
     for (int l = 0; l < VEC; ++l) {
       const int32_t id = k * VEC - cv.hoff + l;
-      const uint32_t kx = gkey<ES>(x[l]);
-      if (id >= 0 && id < V) {
-        if (kx == t) m |= 1u << l;
-        above += kx > t;
-      }
+      if (id >= 0 && id < V && gkey<ES>(x[l]) == t) m |= 1u << l;
     }
     return m;
   };
-  unsigned long long n = 0, na = 0;
+  unsigned long long n = 0;
   for (int32_t kb = k0; kb < k1; kb += 32 * kGUnroll) {
     uint4 w[kGUnroll];
 #pragma unroll
@@ -291,19 +322,13 @@ __device__ __forceinline__ GTie g_tie_id(const unsigned char* row, int32_t V, ui
 #pragma unroll
     for (int u = 0; u < kGUnroll; ++u) {
       const int32_t k = kb + 32 * u + lane;
-      if (k < k1) {
-        unsigned a = 0;
-        n += __popc(scan(w[u], k, a));
-        na += a;
-      }
+      if (k < k1) n += __popc(scan(w[u], k));
     }
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    n += __shfl_xor_sync(0xffffffffu, n, off);
-    na += __shfl_xor_sync(0xffffffffu, na, off);
-  }
+  for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
   if (lane == 0) red[warp] = n;
+  if (threadIdx.x == 0) *shared_id = -1;
   __syncthreads();
   unsigned long long before = 0;
   int owner = -1;
@@ -311,57 +336,63 @@ __device__ __forceinline__ GTie g_tie_id(const unsigned char* row, int32_t V, ui
     if (owner < 0 && before + red[w] >= c) owner = w;
     if (owner < 0) before += red[w];
   }
-  __syncthreads();
-  if (lane == 0) red[warp] = na;
-  if (threadIdx.x == 0) *shared_id = -1;
-  __syncthreads();
-  GTie res;
-  res.n_above = 0;
-  for (int w = 0; w < kGWarps; ++w) res.n_above += red[w];
   if (warp == owner) {
     unsigned long long left = c - before;  // >= 1
-    for (int32_t kb = k0; kb < k1; kb += 32) {
-      const int32_t k = kb + lane;
-      unsigned a = 0;
-      const unsigned m = k < k1 ? scan(g_ld16(cv.base, k), k, a) : 0u;
-      unsigned cnt = __popc(m), incl = cnt;
+    bool found = false;
+    for (int32_t kb = k0; kb < k1 && !found; kb += 32 * kGUnroll) {
+      uint4 w[kGUnroll];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const unsigned y = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += y;
+      for (int u = 0; u < kGUnroll; ++u) {
+        const int32_t k = kb + 32 * u + lane;
+        w[u] = k < k1 ? g_ld16(cv.base, k) : make_uint4(0u, 0u, 0u, 0u);
       }
-      const unsigned hit = __ballot_sync(0xffffffffu, incl >= left && incl - cnt < left);
-      if (hit) {
-        if (lane == __ffs(hit) - 1) {
-          unsigned r = static_cast<unsigned>(left - (incl - cnt));  // r-th tie of this vector
-          unsigned mm = m;
-          for (unsigned i = 1; i < r; ++i) mm &= mm - 1;
-          *shared_id = k * VEC - cv.hoff + (__ffs(mm) - 1);
+#pragma unroll
+      for (int u = 0; u < kGUnroll; ++u) {
+        if (found) break;
+        const int32_t k = kb + 32 * u + lane;
+        const unsigned m = k < k1 ? scan(w[u], k) : 0u;
+        unsigned cnt = __popc(m), incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const unsigned y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
         }
-        break;
+        const unsigned hit = __ballot_sync(0xffffffffu, incl >= left && incl - cnt < left);
+        if (hit) {
+          if (lane == __ffs(hit) - 1) {
+            unsigned r = static_cast<unsigned>(left - (incl - cnt));  // r-th tie of this vector
+            unsigned mm = m;
+            for (unsigned i = 1; i < r; ++i) mm &= mm - 1;
+            *shared_id = k * VEC - cv.hoff + (__ffs(mm) - 1);
+          }
+          found = true;
+        } else {
+          left -= __shfl_sync(0xffffffffu, incl, 31);
+        }
       }
-      left -= __shfl_sync(0xffffffffu, incl, 31);
     }
   }
   __syncthreads();
-  res.id = *shared_id;
+  const int32_t id = *shared_id;
   __syncthreads();
-  return res;
+  return id;
 }
 
-// Shared histograms of counts and fixed-point masses: level 1 (kGBins weight
-// bins; kGWarps / kL1Copies warps share a copy) and the key-digit levels (256
-// bins).
+// Shared histograms (dynamic shared memory): level 1 (kGBins weight bins,
+// counts and scaled masses in 32 bits; kGWarps / kL1Copies warps share a
+// copy) and the key-digit levels (256 bins, counts and exact fixed-point
+// masses, one private copy per warp).
 struct GHist {
-  unsigned long long l1m[kL1Copies][kGBins];
   uint32_t l1n[kL1Copies][kGBins];
-  unsigned long long dm[kDCopies][256];
-  uint32_t dn[kDCopies][256];
+  uint32_t l1s[kL1Copies][kGBins];  // sum of w >> gshift(b)
+  unsigned long long dm[kGWarps][256];
+  uint32_t dn[kGWarps][256];
 };
 
-// Warp-aggregated histogram update: every lane with d >= 0 adds one to count
-// bin d and w to mass bin d, the lanes of a warp that share a bin with one
-// atomic per bin.  All 32 lanes of the warp call it.
+// Warp-aggregated update of the warp's own histogram: every lane with d >= 0
+// adds one to count bin d and w to mass bin d; the lanes that share a bin
+// add together, through one lane, so no other lane writes that bin meanwhile
+// and plain stores suffice.  All 32 lanes of the warp call it.
 __device__ __forceinline__ void g_add_agg(uint32_t* n, unsigned long long* m, int d,
                                           unsigned long long w) {
   const int lane = threadIdx.x & 31;
@@ -375,27 +406,34 @@ __device__ __forceinline__ void g_add_agg(uint32_t* n, unsigned long long* m, in
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
     if (lane == src) {
-      atomicAdd(n + ds, static_cast<uint32_t>(__popc(grp)));
-      if (s) atomicAdd(m + ds, s);
+      n[ds] += static_cast<uint32_t>(__popc(grp));
+      m[ds] += s;
     }
+    __syncwarp();
     todo &= ~grp;
   }
 }
 
 // Warp 0 only: over NB bins in order (j = 0 first along the value-desc
 // order; bin_n / bin_m give a bin's count and mass), the first bin at which
-// the cumulative count (by_mass false) or mass reaches need.  Writes the bin,
-// the count and the mass of the bins before it and the bin's count to
-// out[0..3].
+// the cumulative count (by_mass false) or mass reaches need (the last bin if
+// none does), with the count and mass of the bins before it and its count;
+// every lane of the warp gets the result.
+struct GFound {
+  int j;
+  unsigned long long n_before, m_before, n_bin;
+};
+
 template <int NB, typename FN, typename FM>
-__device__ __forceinline__ void g_find(FN&& bin_n, FM&& bin_m, bool by_mass,
-                                       unsigned long long need, unsigned long long* out) {
+__device__ __forceinline__ GFound g_find(FN&& bin_n, FM&& bin_m, bool by_mass,
+                                         unsigned long long need) {
   constexpr int PER = NB / 32;
   const int lane = threadIdx.x & 31;
   unsigned long long ln = 0, lm = 0;
-  for (int i = 0; i < PER; ++i) {
-    ln += bin_n(lane * PER + i);
-    lm += bin_m(lane * PER + i);
+  for (int i = 0; i < PER; ++i) {  // the lane's bins in rotated order: few bank conflicts
+    const int j = lane * PER + ((i + lane) & (PER - 1));
+    ln += bin_n(j);
+    lm += bin_m(j);
   }
   unsigned long long in = ln, im = lm;  // inclusive scans over lanes
 #pragma unroll
@@ -408,74 +446,127 @@ __device__ __forceinline__ void g_find(FN&& bin_n, FM&& bin_m, bool by_mass,
     }
   }
   const unsigned rl = __ballot_sync(0xffffffffu, (by_mass ? im : in) >= need);
-  const int L = rl ? __ffs(rl) - 1 : 31;  // need is within the total
+  const int L = rl ? __ffs(rl) - 1 : 31;
+  GFound f{L * PER + PER - 1, 0, 0, 0};
   if (lane == L) {
     unsigned long long an = in - ln, am = im - lm;  // bins of earlier lanes
     for (int i = 0; i < PER; ++i) {
       const int j = L * PER + i;
       const unsigned long long cn = bin_n(j), cm = bin_m(j);
       if ((by_mass ? am + cm : an + cn) >= need || i == PER - 1) {
-        out[0] = static_cast<unsigned long long>(j);
-        out[1] = an;
-        out[2] = am;
-        out[3] = cn;
+        f = GFound{j, an, am, cn};
         break;
       }
       an += cn;
       am += cm;
     }
   }
+  f.j = __shfl_sync(0xffffffffu, f.j, L);
+  f.n_before = __shfl_sync(0xffffffffu, f.n_before, L);
+  f.m_before = __shfl_sync(0xffffffffu, f.m_before, L);
+  f.n_bin = __shfl_sync(0xffffffffu, f.n_bin, L);
+  return f;
 }
 
-// Search along the (value desc, id asc) order inside level-1 bin b: the value
-// key t of the element at which the cumulative count (by_mass false) or mass
-// of the bin's elements reaches need (>= 1, at most the bin's total), the
-// count and mass of the bin's keys above t, and the count of keys equal to t.
-// One pass per 8-bit digit of the key (two for bf16, four for fp32), each a
-// histogram of the bin's elements matching the digits chosen so far.
+// Search along the (value desc, id asc) order inside the run of level-1 bins
+// [ba, bb]: the value key t of the element at which the cumulative count
+// (by_mass false) or mass reaches the target, the count and mass of the
+// run's keys above t, the count of keys equal to t, and the exact mass of the
+// bins before ba (summed in the first pass).  By count, need is the count
+// still needed from the run; by mass, it is the target itself, reached
+// inside the run.  One pass per 8-bit digit of the key (two for bf16, four
+// for fp32), each a histogram of the run's elements matching the digits
+// chosen so far.
 struct GSel {
   uint32_t t;
-  unsigned long long n_above, m_above, ties;
+  unsigned long long n_above, m_above, ties, m_before;
 };
 
 template <int ES>
 __device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, float sc, float h,
-                                         int b, unsigned long long need, bool by_mass,
+                                         int ba, int bb, unsigned long long need, bool by_mass,
                                          GHist* hist, unsigned long long* red) {
   constexpr int W = ES == 2 ? 16 : 32;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  const int cd = warp % kDCopies;
+  constexpr int VEC = 16 / ES, kGUnroll = g_unroll<ES>(), NE = kGUnroll * VEC;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const GCover cv = g_cover<ES>(row, V);
   uint32_t prefix = 0;
   GSel res{};
   for (int shift = W - 8; shift >= 0; shift -= 8) {
-    for (int i = tid; i < kDCopies * 256; i += kGThreads) {
+    const bool first = shift + 8 >= W;
+    for (int i = tid; i < kGWarps * 256; i += kGThreads) {
       (&hist->dn[0][0])[i] = 0;
       (&hist->dm[0][0])[i] = 0;
     }
     __syncthreads();
-    g_for_row<ES>(row, V, [&](int32_t, float x, bool ok) {
-      const float y = fmaf(x, sc, -h);
-      const uint32_t k = gkey<ES>(x);
-      const bool in = ok && gbin(y) == b && (k >> shift >> 8) == prefix;
-      const unsigned long long w = in ? __float2ull_rn(ex2(y) * kGFix) : 0ull;
-      g_add_agg(hist->dn[cd], hist->dm[cd], in ? static_cast<int>((k >> shift) & 255u) : -1, w);
-    });
+    // a round: kGUnroll vectors a lane (16 logits); the per-logit tests
+    // first, the warp-aggregated updates only when some lane of the warp
+    // holds a logit of the run
+    unsigned long long mb = 0;  // the thread's share of the mass before the run
+    for (int32_t k0 = tid - lane; k0 < cv.nvec; k0 += kGUnroll * kGThreads) {
+      uint4 wv[kGUnroll];
+#pragma unroll
+      for (int u = 0; u < kGUnroll; ++u) {
+        const int32_t k = k0 + u * kGThreads + lane;
+        wv[u] = k < cv.nvec ? g_ld16(cv.base, k) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      float x[NE];
+#pragma unroll
+      for (int u = 0; u < kGUnroll; ++u) g_unpack<ES>(wv[u], x + u * VEC);
+      uint32_t inm = 0;
+#pragma unroll
+      for (int e = 0; e < NE; ++e) {
+        const int32_t k = k0 + (e / VEC) * kGThreads + lane;
+        const int32_t id = k * VEC - cv.hoff + e % VEC;
+        const bool ok = k < cv.nvec && id >= 0 && id < V;
+        const float y = fmaf(x[e], sc, -h);
+        const int bx = gbin(y);
+        if (ok && bx >= ba && bx <= bb && (gkey<ES>(x[e]) >> shift >> 8) == prefix) inm |= 1u << e;
+        if (first && ok && bx < ba) mb += gweight_y(y);
+      }
+      if (__any_sync(0xffffffffu, inm != 0)) {
+#pragma unroll
+        for (int e = 0; e < NE; ++e) {
+          const bool in = (inm >> e) & 1u;
+          g_add_agg(hist->dn[warp], hist->dm[warp],
+                    in ? static_cast<int>((gkey<ES>(x[e]) >> shift) & 255u) : -1,
+                    in ? gweight_y(fmaf(x[e], sc, -h)) : 0ull);
+        }
+      }
+    }
     __syncthreads();
+    {  // the warps' histograms summed into warp 0's: counts by threads 0..255,
+       // masses by threads 256..511, one bin each
+      const int j = tid & 255;
+      if (tid < 256) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int q = 0; q < kGWarps; ++q) c += hist->dn[q][j];
+        hist->dn[0][j] = c;
+      } else {
+        unsigned long long m = 0;
+#pragma unroll
+        for (int q = 0; q < kGWarps; ++q) m += hist->dm[q][j];
+        hist->dm[0][j] = m;
+      }
+    }
+    if (first) {
+      res.m_before = g_sum_u64(mb, red);  // its barriers also order the sums above
+      if (by_mass) need -= res.m_before;  // >= 1: the bins before ba hold less than the target
+    } else {
+      __syncthreads();
+    }
     if (warp == 0) {
-      g_find<256>(
-          [&](int j) {
-            unsigned long long s = 0;
-#pragma unroll
-            for (int c = 0; c < kDCopies; ++c) s += hist->dn[c][255 - j];
-            return s;
-          },
-          [&](int j) {
-            unsigned long long s = 0;
-#pragma unroll
-            for (int c = 0; c < kDCopies; ++c) s += hist->dm[c][255 - j];
-            return s;
-          },
-          by_mass, need, red);
+      const GFound f = g_find<256>(
+          [&](int j) { return static_cast<unsigned long long>(hist->dn[0][255 - j]); },
+          [&](int j) { return hist->dm[0][255 - j]; },
+          by_mass, need);
+      if (lane == 0) {
+        red[0] = static_cast<unsigned long long>(f.j);
+        red[1] = f.n_before;
+        red[2] = f.m_before;
+        red[3] = f.n_bin;
+      }
     }
     __syncthreads();
     prefix = (prefix << 8) | (255u - static_cast<uint32_t>(red[0]));
@@ -528,84 +619,101 @@ __device__ __forceinline__ GRow g_select_row(const Params& P, const unsigned cha
   if (g.flags) {  // no distribution: keep the argmax alone
     g.thr_key = 0xffffffffu;
     g.z = 1.f;
-    g.n_kept = 1;
     return g;
   }
   const float h = g.h;
   const bool use_k = P.top_k > 0 && P.top_k < V;
   const bool use_p = P.top_p < 1.f;
-  // ---- level 1, one pass: masses (and, for top-k, counts) of the weight bins
+  const int lane = tid & 31;
+  // ---- level 1, one pass: counts and scaled masses of the weight bins
+  //      (32-bit shared atomics), and the row's exact mass from the threads'
+  //      own sums
   const int c1 = warp % kL1Copies;
   for (int i = tid; i < kL1Copies * kGBins; i += kGThreads) {
     (&hist->l1n[0][0])[i] = 0;
-    (&hist->l1m[0][0])[i] = 0;
+    (&hist->l1s[0][0])[i] = 0;
   }
   __syncthreads();
+  unsigned long long zs = 0;
   g_for_row<ES>(row, V, [&](int32_t, float x, bool ok) {
     if (!ok) return;
     const float y = fmaf(x, sc, -h);
     const int b = gbin(y);
-    if (use_k) atomicAdd(&hist->l1n[c1][b], 1u);
-    const unsigned long long w = __float2ull_rn(ex2(y) * kGFix);
-    if (w) atomicAdd(&hist->l1m[c1][b], w);
+    const unsigned long long w = gweight_y(y);
+    zs += w;
+    atomicAdd(&hist->l1n[c1][b], 1u);
+    const uint32_t ws = static_cast<uint32_t>(w >> gshift(b));
+    if (ws) atomicAdd(&hist->l1s[c1][b], ws);
   });
   __syncthreads();
+  const unsigned long long zt = g_sum_u64(zs, red);  // the row's total mass
   auto l1n = [&](int j) {
-    unsigned long long s = 0;
+    unsigned long long c = 0;
 #pragma unroll
-    for (int c = 0; c < kL1Copies; ++c) s += hist->l1n[c][j];
-    return s;
+    for (int q = 0; q < kL1Copies; ++q) c += hist->l1n[q][j];
+    return c;
   };
-  auto l1m = [&](int j) {
-    unsigned long long s = 0;
+  auto l1lo = [&](int j) {  // lower bound of bin j's mass
+    unsigned long long m = 0;
 #pragma unroll
-    for (int c = 0; c < kL1Copies; ++c) s += hist->l1m[c][j];
-    return s;
+    for (int q = 0; q < kL1Copies; ++q) m += hist->l1s[q][j];
+    return m << gshift(j);
   };
-  unsigned long long zt = 0;  // the row's total mass
-  for (int j = tid; j < kGBins; j += kGThreads) zt += l1m(j);
-  zt = g_sum_u64(zt, red);
+  auto l1hi = [&](int j) { return l1lo(j) + (l1n(j) << gshift(j)); };  // upper bound
   unsigned long long zk = zt;  // mass of the kept set
   if (use_k) {
-    // ---- top-k: the bin holding the k-th element by count, then its key
-    //      digits; the kept mass from the bins and digits above and the tie
-    //      weight (every tie weighs the same)
+    // ---- top-k: the bin holding the k-th element by count (exact), then its
+    //      key digits; the kept mass from the mass before the bin, the
+    //      digits above and the tie weight (every tie weighs the same)
     const unsigned long long k = static_cast<unsigned long long>(P.top_k);
-    if (warp == 0) g_find<kGBins>(l1n, l1m, false, k, red);
+    if (warp == 0) {
+      const GFound f = g_find<kGBins>(l1n, l1lo, false, k);
+      if (lane == 0) {
+        red[0] = static_cast<unsigned long long>(f.j);
+        red[1] = f.n_before;
+      }
+    }
     __syncthreads();
     const int bk = static_cast<int>(red[0]);
-    const unsigned long long nb = red[1], mb = red[2];
+    const unsigned long long nb = red[1];
     __syncthreads();
-    const GSel s = g_digits<ES>(row, V, sc, h, bk, k - nb, false, hist, red);
-    const unsigned long long n_above = nb + s.n_above;
-    const unsigned long long ck = k - n_above;  // 1 <= ck <= ties
+    const GSel s = g_digits<ES>(row, V, sc, h, bk, bk, k - nb, false, hist, red);
+    const unsigned long long ck = k - (nb + s.n_above);  // 1 <= ck <= ties
     const unsigned long long wt = gweight(gkey_value<ES>(s.t), sc, h);
-    zk = mb + s.m_above + ck * wt;
+    zk = s.m_before + s.m_above + ck * wt;
     g.thr_key = s.t;
-    g.n_kept = static_cast<int32_t>(n_above + ck);
-    if (!use_p) g.thr_id = g_tie_id<ES>(row, V, s.t, ck, red, sid).id;
+    if (!use_p) g.thr_id = g_tie_id<ES>(row, V, s.t, ck, red, sid);
   }
   if (use_p) {
     // ---- top-p: the shortest prefix of the order whose mass reaches top_p *
     //      zk (integers: the first prefix with mass >= ceil(top_p * zk)); the
     //      top-k set is itself a prefix of the order holding zk >= that, so the
-    //      search runs over the whole row and stops inside it
+    //      search runs over the whole row and stops inside it.  The level-1
+    //      bounds place the crossing inside the run of bins [ba, bb]: ba the
+    //      first bin whose cumulative upper bound reaches the target, bb the
+    //      first whose cumulative lower bound does (one bin but for targets
+    //      within about 2^-13 of a bin edge).
     const unsigned long long target = max(1ull, static_cast<unsigned long long>(
         ceil(static_cast<double>(P.top_p) * static_cast<double>(zk))));
-    if (warp == 0) g_find<kGBins>(l1n, l1m, true, target, red);
+    if (warp == 0) {
+      auto none = [](int) { return 0ull; };
+      const GFound fa = g_find<kGBins>(none, l1hi, true, target);
+      const GFound fb = g_find<kGBins>(none, l1lo, true, target);
+      if (lane == 0) {
+        red[0] = static_cast<unsigned long long>(fa.j);
+        red[1] = static_cast<unsigned long long>(max(fa.j, fb.j));
+      }
+    }
     __syncthreads();
-    const int bp = static_cast<int>(red[0]);
-    const unsigned long long mb = red[2];
+    const int ba = static_cast<int>(red[0]), bb = static_cast<int>(red[1]);
     __syncthreads();
-    const GSel s = g_digits<ES>(row, V, sc, h, bp, target - mb, true, hist, red);
-    const unsigned long long m_above = mb + s.m_above;
+    const GSel s = g_digits<ES>(row, V, sc, h, ba, bb, target, true, hist, red);
+    const unsigned long long m_above = s.m_before + s.m_above;
     const unsigned long long wt = gweight(gkey_value<ES>(s.t), sc, h);
     unsigned long long cp = wt > 0 ? (target - m_above + wt - 1) / wt : s.ties;
     cp = max(1ull, min(cp, s.ties));
-    const GTie tie = g_tie_id<ES>(row, V, s.t, cp, red, sid);
     g.thr_key = s.t;
-    g.thr_id = tie.id;
-    g.n_kept = static_cast<int32_t>(tie.n_above + cp);
+    g.thr_id = g_tie_id<ES>(row, V, s.t, cp, red, sid);
     zk = m_above + cp * wt;
   }
   g.z = static_cast<float>(static_cast<double>(zk) / static_cast<double>(kGFix));
@@ -622,7 +730,9 @@ template <int ES>
 __global__ void __launch_bounds__(kGThreads, 2) gfilter_rows_kernel(const Params P) {
   __shared__ unsigned long long red[kGWarps];
   __shared__ int32_t sid;
-  __shared__ GHist hist;
+  extern __shared__ __align__(16) unsigned char g_dyn[];
+  GHist& hist = *reinterpret_cast<GHist*>(g_dyn);  // sizeof(GHist) bytes of dynamic shared memory
+  __shared__ GRow s_gt;  // the target row's record while its partner is selected
   grid_dep_launch_dependents();
   auto slot = [&](int32_t i) {  // row i's record, at FiltRow stride
     return reinterpret_cast<GRow*>(reinterpret_cast<FiltRow*>(P.filt) + i);
@@ -639,19 +749,27 @@ __global__ void __launch_bounds__(kGThreads, 2) gfilter_rows_kernel(const Params
     const int32_t gd = g - r;
     const bool pair = off <= g && g < off1 - 1 && gd >= 0 && gd < P.Nd;
     const unsigned char* trow = P.tgt + static_cast<size_t>(g) * P.V * ES;
-    const GRow gt = g_select_row<ES>(P, trow, red, &sid, &hist);
+    {
+      const GRow t = g_select_row<ES>(P, trow, red, &sid, &hist);
+      if (threadIdx.x == 0) s_gt = t;
+    }
+    __syncthreads();
     GRow gdr{};
-    int fl = gt.flags;
+    int fl = s_gt.flags;
     int acc = 0;
     if (pair) {
       const unsigned char* drow = P.drf + static_cast<size_t>(gd) * P.V * ES;
       gdr = g_select_row<ES>(P, drow, red, &sid, &hist);
+      const GRow gt = s_gt;
       fl |= gdr.flags;
       // label: sum over both kept sets of min(p_t, p_d), element by element
       float part = 0.f;
       if (P.out_conf != nullptr && !fl) {
+        // min(p_t, p_d) is 0 unless both rows keep the token: keys first
+        const float it = 1.f / gt.z, id = 1.f / gdr.z;
         g_for_pair<ES>(trow, drow, P.V, [&](int32_t v, float t, float d) {
-          part += fminf(g_p<ES>(gt, t, v, P.sc), g_p<ES>(gdr, d, v, P.sc));
+          if (gkept(gt, gkey<ES>(t), v) && gkept(gdr, gkey<ES>(d), v))
+            part += fminf(ex2(fmaf(t, P.sc, -gt.h)) * it, ex2(fmaf(d, P.sc, -gdr.h)) * id);
         });
       }
       const float label = g_sum_f32(part, reinterpret_cast<float*>(red));
@@ -670,6 +788,7 @@ __global__ void __launch_bounds__(kGThreads, 2) gfilter_rows_kernel(const Params
       if (threadIdx.x == 0 && P.out_conf != nullptr) P.out_conf[gd] = label;
     }
     if (threadIdx.x == 0) {
+      const GRow gt = s_gt;
       *slot(g) = gt;
       if (pair) *slot(P.Nt + gd) = gdr;
       RowRec rr{};
