@@ -475,8 +475,8 @@ __device__ __forceinline__ GFound g_find(FN&& bin_n, FM&& bin_m, bool by_mass,
 // bins before ba (summed in the first pass).  By count, need is the count
 // still needed from the run; by mass, it is the target itself, reached
 // inside the run.  One pass per 8-bit digit of the key (two for bf16, four
-// for fp32), each a histogram of the run's elements matching the digits
-// chosen so far.
+// for fp32; one for a bf16 run of at most 256 keys), each a histogram of the
+// run's elements matching the digits chosen so far.
 struct GSel {
   uint32_t t;
   unsigned long long n_above, m_above, ties, m_before;
@@ -490,10 +490,34 @@ __device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, fl
   constexpr int VEC = 16 / ES, kGUnroll = g_unroll<ES>(), NE = kGUnroll * VEC;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const GCover cv = g_cover<ES>(row, V);
+  // bf16: the run's keys fill the interval [klo, khi] (the bin never rises
+  // along the key order, from -inf to +inf); found by bisection over the
+  // keys, and when it spans at most 256 keys one level with digit key - klo
+  // replaces the two byte levels.  Digits are taken of key - base (base klo
+  // for the one level, else 0; keys below base wrap and match no prefix).
+  uint32_t klo = 0;
+  bool single = false;
+  if (ES == 2) {
+    auto G = [&](uint32_t k) { return gbin(fmaf(gkey_value<ES>(k), sc, -h)); };
+    uint32_t lo = 0x007fu, hi = 0xff80u;  // the smallest key with G <= bb
+    while (lo < hi) {
+      const uint32_t mid = (lo + hi) >> 1;
+      if (G(mid) <= bb) hi = mid; else lo = mid + 1;
+    }
+    klo = lo;
+    lo = 0x007fu;
+    hi = 0xff80u;  // the largest key with G >= ba
+    while (lo < hi) {
+      const uint32_t mid = (lo + hi + 1) >> 1;
+      if (G(mid) >= ba) lo = mid; else hi = mid - 1;
+    }
+    single = lo >= klo && lo - klo < 256u;
+  }
+  const uint32_t base = single ? klo : 0u;
   uint32_t prefix = 0;
   GSel res{};
-  for (int shift = W - 8; shift >= 0; shift -= 8) {
-    const bool first = shift + 8 >= W;
+  bool first = true;
+  for (int shift = single ? 0 : W - 8; shift >= 0; shift -= 8) {
     for (int i = tid; i < kGWarps * 256; i += kGThreads) {
       (&hist->dn[0][0])[i] = 0;
       (&hist->dm[0][0])[i] = 0;
@@ -521,7 +545,8 @@ __device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, fl
         const bool ok = k < cv.nvec && id >= 0 && id < V;
         const float y = fmaf(x[e], sc, -h);
         const int bx = gbin(y);
-        if (ok && bx >= ba && bx <= bb && (gkey<ES>(x[e]) >> shift >> 8) == prefix) inm |= 1u << e;
+        if (ok && bx >= ba && bx <= bb && ((gkey<ES>(x[e]) - base) >> shift >> 8) == prefix)
+          inm |= 1u << e;
         if (first && ok && bx < ba) mb += gweight_y(y);
       }
       if (__any_sync(0xffffffffu, inm != 0)) {
@@ -529,7 +554,7 @@ __device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, fl
         for (int e = 0; e < NE; ++e) {
           const bool in = (inm >> e) & 1u;
           g_add_agg(hist->dn[warp], hist->dm[warp],
-                    in ? static_cast<int>((gkey<ES>(x[e]) >> shift) & 255u) : -1,
+                    in ? static_cast<int>(((gkey<ES>(x[e]) - base) >> shift) & 255u) : -1,
                     in ? gweight_y(fmaf(x[e], sc, -h)) : 0ull);
         }
       }
@@ -574,9 +599,10 @@ __device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, fl
     res.m_above += red[2];
     res.ties = red[3];
     need -= by_mass ? red[2] : red[1];
+    first = false;
     __syncthreads();
   }
-  res.t = prefix;
+  res.t = base + prefix;
   return res;
 }
 
