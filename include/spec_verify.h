@@ -126,9 +126,10 @@ size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows);
  *                 kept-set path: one pass per row selects the set exactly,
  *                 then one warp per request decides on it.  Larger kept
  *                 sets (top_k above 64, or top_p over the whole vocabulary)
- *                 run the general path: per row a bisection over the value
- *                 key with exact fixed-point mass sums finds the kept set's
- *                 threshold, then one CTA per request decides and draws.
+ *                 run the general path: per row a search over weight bins
+ *                 and key digits with exact fixed-point mass sums finds the
+ *                 kept set's threshold, then one CTA per request decides
+ *                 and draws.
  *  mode           SV_GREEDY or SV_SAMPLE.
  *  out_tokens     [N_t] int32 device: for request r, entries off_r .. off_r
  *                 + a_r - 1 = accepted drafts, entry off_r + a_r = the final

@@ -12,16 +12,18 @@
 //
 // Both thresholds come from one search scheme along that order, exact and
 // independent of the visiting order.  Weights w = exp2(x sc - h) (h = x_max
-// sc) are summed as fixed-point integers of 2^-40.  Level 1 is one pass: a
-// histogram of masses (and, for top-k, counts) over weight bins, eighths of
-// a binade of w, which are runs of the order and spread a row's tokens
-// thinly (few lanes of a warp meet on one bin).  The bin where the
-// cumulative count reaches k, or the cumulative mass reaches
-// ceil(top_p * kept mass), is then searched by the key's 8-bit digits (two
-// passes for bf16, four for fp32) over that bin's tokens only, with
-// warp-aggregated updates.  Inside the tie class of the final value every
-// token weighs the same, so the cut falls after c of them, c from integer
-// arithmetic; a counting pass finds the id of the c-th.
+// sc) are fixed-point integers of 2^-40.  Level 1 is one pass: per weight
+// bin (eighths of a binade of w; each bin a run of the order, and a row's
+// tokens spread thinly over them) a count and a mass scaled down to 32 bits,
+// which bound the bin's exact mass; the row's exact total comes from the
+// threads' own sums.  The bin where the cumulative count reaches k, or the
+// run of bins where the bounded cumulative mass reaches ceil(top_p * kept
+// mass), is then searched by key digits over that run's tokens only (one
+// pass for a bf16 run of at most 256 keys, else one per 8-bit digit), with
+// warp-aggregated updates of per-warp histograms; the first of those passes
+// also sums the exact mass before the run.  Inside the tie class of the
+// final value every token weighs the same, so the cut falls after c of them,
+// c from integer arithmetic; a counting pass finds the id of the c-th.
 //
 //  gfilter_rows_kernel      one CTA per target row: the kept sets of the row
 //                           and of its draft partner, the label
@@ -116,18 +118,6 @@ __device__ __forceinline__ unsigned long long g_sum_u64(unsigned long long v,
   __syncthreads();
   unsigned long long t = 0;
   for (int w = 0; w < kGWarps; ++w) t += red[w];
-  __syncthreads();
-  return t;
-}
-
-__device__ __forceinline__ unsigned long long g_max_u64(unsigned long long v,
-                                                        unsigned long long* red) {
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, off));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  unsigned long long t = 0;
-  for (int w = 0; w < kGWarps; ++w) t = max(t, red[w]);
   __syncthreads();
   return t;
 }

@@ -415,7 +415,7 @@ def test_filtered_ties_take_lowest_ids(cuda_lib):
 
 
 # kept sets of any size: top_k above SV_MAX_FILTER_K, top-p over the whole
-# vocabulary (the bisection path).  Cases whose top-p cuts sit clear of the
+# vocabulary (the general path).  Cases whose top-p cuts sit clear of the
 # near-tie margin (kept sets of about 60 to 1,100 tokens at T = 1; smaller
 # at T < 1 with the +8 peak); a cut whose boundary token has probability
 # near 1e-5 is fragile at fp32 precision and counted as a near tie.
