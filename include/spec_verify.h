@@ -129,7 +129,8 @@ size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows);
  *                 run the general path: per row a search over weight bins
  *                 and key digits with exact fixed-point mass sums finds the
  *                 kept set's threshold, then one CTA per request decides
- *                 and draws.
+ *                 and draws.  The general path takes V up to 2^21 (else
+ *                 SV_ERR_UNSUPPORTED).
  *  mode           SV_GREEDY or SV_SAMPLE.
  *  out_tokens     [N_t] int32 device: for request r, entries off_r .. off_r
  *                 + a_r - 1 = accepted drafts, entry off_r + a_r = the final

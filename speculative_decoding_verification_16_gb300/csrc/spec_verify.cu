@@ -218,6 +218,8 @@ int check_args(const Args& a) {
     if (p && !aligned(p, 4)) return SV_ERR_ARG;
   const int es = a.dtype == SV_BF16 ? 2 : 4;
   if (static_cast<double>(a.n_target_rows) * a.V * es > 9.0e18) return SV_ERR_ARG;
+  // the general filter path sums level-1 masses in 32 bits, exact up to kGMaxV
+  if (filter_k(a.V, a.top_k, a.top_p) < 0 && a.V > kGMaxV) return SV_ERR_UNSUPPORTED;
   if (a.workspace == nullptr || !aligned(a.workspace, 256) ||
       a.workspace_bytes < spec_verify_workspace_size(a.B, a.n_target_rows))
     return SV_ERR_WORKSPACE;

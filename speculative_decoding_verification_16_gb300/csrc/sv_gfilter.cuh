@@ -52,6 +52,7 @@ template <int ES>
 __host__ __device__ constexpr int g_unroll() { return ES == 2 ? 2 : 4; }
 constexpr int kGBins = 512;    // level-1 bins: eighths of a binade of the weight
 constexpr int kL1Copies = 4;   // level-1 histogram copies
+constexpr int kGMaxV = 1 << 21;  // largest V the 32-bit level-1 masses take (gshift)
 
 // A row's kept set and statistics (stored in the row's FiltRow slot of the
 // workspace).

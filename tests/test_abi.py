@@ -97,6 +97,7 @@ def _call(lib, **over):
     (dict(ws=None), -5),
     (dict(ws=(1 << 20) + 128), -5),   # workspace must be 256-byte aligned
     (dict(ws_bytes=64), -5),
+    (dict(V=(1 << 21) + 8, top_p=0.9), -4),  # general filter path beyond its V limit
 ])
 def test_host_argument_checks(lib, over, code):
     assert _call(lib, **over) == code
