@@ -259,6 +259,16 @@ def test_topk_topp_bruteforce():
         assert got.p.sum() == pytest.approx(1.0, abs=1e-12)
 
 
+def test_signed_zeros_tie_by_id():
+    """Reading 7: -0 and +0 are one value, so a top-k cut inside a class of
+    zero logits keeps the lowest ids whatever their signs."""
+    x = np.array([-1.0, -0.0, 0.0, -0.0, 0.0, -2.0])
+    got = oracle.process_row(x, 1.0, 3, 1.0)
+    assert np.flatnonzero(got.p > 0).tolist() == [1, 2, 3]
+    np.testing.assert_allclose(got.p[[1, 2, 3]], 1.0 / 3.0, rtol=0, atol=1e-15)
+    assert got.argmax == 1  # lowest id holding the maximum
+
+
 def test_final_pick_matches_loop():
     rng = np.random.default_rng(8)
     for _ in range(500):
