@@ -15,6 +15,10 @@ from .spec_verify_oracle import (  # noqa: F401
     process_row,
     pair_step,
     final_pick,
+    pick_admissible,
+    topp_sizes,
+    row_alternatives,
+    admissible_outcomes,
     decide_request,
     conf_label,
     Processed,

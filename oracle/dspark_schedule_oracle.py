@@ -18,7 +18,7 @@ What it computes ("DeepSeek DSpark speculative decoding" tutorial):
   candidate tokens by cumulative survival probability, descending; add them
   one at a time, recomputing Theta; stop as soon as Theta no longer rises.
 
-Readings where the pages are silent (each one is also listed in the design doc):
+Readings where the pages are silent:
 
 * tau is the expected number of tokens one verify step produces: one per
   request (the replacement or bonus token) plus each verified draft k,

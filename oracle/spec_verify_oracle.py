@@ -28,7 +28,7 @@ What it computes, and where each step comes from (page title, section):
 * Sampling parameters temperature, top_p, top_k (DSpine page, "加速效果":
   temperature 1.0, top_p 0.95, top_k 20).
 
-Readings where the pages are silent (each one is also listed in the design doc):
+Readings where the pages are silent:
 
 * Filter order: z = logit / T; keep the top_k tokens by (z desc, id asc);
   renormalise; keep the shortest prefix of that same order whose
@@ -51,8 +51,16 @@ Readings where the pages are silent (each one is also listed in the design doc):
   near-tied choice): every decision records its margin in absolute
   probability units -- |u - p_t/p_d| for the accept test,
   |cumsum_b - u*R| at the two edges of the chosen interval for an inverse
-  CDF, |cumsum_b - top_p| at the two edges of a top-p cut.  A request with
-  any margin below NEAR_TIE is reported as near-tied.
+  CDF, |cumsum_b - top_p| at the two edges of a top-p cut, and the residual
+  mass R itself for the choice between the residual and p_t at a rejection
+  (the rule switches to p_t at R = 0; an exact zero is no near tie, since
+  then p_t = p_d and both branches draw from the same distribution).  A
+  request with any margin below NEAR_TIE is reported as near-tied.
+* What a near tie leaves open: ``admissible_outcomes`` lists every result
+  the rules give when each cumulative sum, ratio and residual mass may move
+  by up to NEAR_TIE: the top-p kept-set sizes of every row, whether the
+  accept chain is fixed, and the set of final tokens.  A computation in
+  lower precision is correct when its result is one of these.
 """
 
 from __future__ import annotations
@@ -85,24 +93,44 @@ def decode_logits(raw, dtype: str) -> np.ndarray:
 class Processed:
     """One processed row: probabilities and the statistics reported for parity."""
 
-    __slots__ = ("p", "m", "Z", "argmax", "topp_margin", "n_kept")
+    __slots__ = ("p", "m", "Z", "argmax", "topp_margin", "n_kept", "topp_sizes")
 
-    def __init__(self, p, m, Z, argmax, topp_margin, n_kept):
+    def __init__(self, p, m, Z, argmax, topp_margin, n_kept, topp_sizes=None):
         self.p = p
         self.m = m
         self.Z = Z
         self.argmax = argmax
         self.topp_margin = topp_margin
         self.n_kept = n_kept
+        # kept-set sizes a top-p cut could take within the near-tie band
+        # (just n_kept when no cut is near a boundary or top-p is off)
+        self.topp_sizes = [n_kept] if topp_sizes is None else topp_sizes
 
 
-def process_row(x: np.ndarray, temperature: float, top_k: int, top_p: float) -> Processed:
+def topp_sizes(cum, top_p: float, tol: float):
+    """Kept-set sizes n' that the top-p rule "shortest prefix whose cumulative
+    probability reaches top_p" gives when the cumulative sums may move by up
+    to ``tol``: cum[n'-1] >= top_p - tol, and the prefix one shorter does
+    not reach top_p + tol (cum[n'-2] < top_p + tol; nothing to check for
+    n' = 1).  ``cum`` is the cumulative probability along the (value desc,
+    id asc) order."""
+    sizes = []
+    for n in range(1, len(cum) + 1):
+        if cum[n - 1] >= top_p - tol and (n == 1 or cum[n - 2] < top_p + tol):
+            sizes.append(n)
+    return sizes or [len(cum)]
+
+
+def process_row(x: np.ndarray, temperature: float, top_k: int, top_p: float,
+                keep_n: int | None = None) -> Processed:
     """Temperature, then top-k, renormalise, then top-p, renormalise.
 
     ``x`` is one row of logits in float64.  NaN or +inf anywhere, or a row
     that is entirely -inf, has no distribution and raises ValueError.
     With ``temperature <= 0`` only the argmax is defined (greedy decisions
-    need nothing else); p, m and Z are then None.
+    need nothing else); p, m and Z are then None.  ``keep_n`` replaces the
+    top-p prefix length by a given one (one of ``topp_sizes``; used to list
+    what a near-tied cut leaves open).
     """
     x = np.asarray(x, dtype=np.float64)
     V = x.size
@@ -129,6 +157,7 @@ def process_row(x: np.ndarray, temperature: float, top_k: int, top_p: float) -> 
     kept = order[:top_k] if use_k else order
     w = np.exp(z[kept] - m)
     margin = np.inf
+    sizes = None
     if use_p:
         cum = np.cumsum(w / w.sum())
         reach = np.flatnonzero(cum >= top_p)
@@ -136,12 +165,27 @@ def process_row(x: np.ndarray, temperature: float, top_k: int, top_p: float) -> 
         margin = abs(cum[n - 1] - top_p)
         if n >= 2:
             margin = min(margin, abs(cum[n - 2] - top_p))
+        sizes = topp_sizes(cum, top_p, NEAR_TIE)
+        if keep_n is not None:
+            n = int(keep_n)
         kept = kept[:n]
         w = w[:n]
     Z = w.sum()
     p = np.zeros(V)
     p[kept] = w / Z
-    return Processed(p, m, Z, argmax, margin, kept.size)
+    return Processed(p, m, Z, argmax, margin, kept.size, sizes)
+
+
+def row_alternatives(x: np.ndarray, temperature: float, top_k: int, top_p: float):
+    """Every processed form of one row that a top-p cut within the near-tie
+    band allows (one entry when the cut is clear of it): the oracle's own
+    choice first."""
+    first = process_row(x, temperature, top_k, top_p)
+    alts = [first]
+    for n in first.topp_sizes:
+        if n != first.n_kept:
+            alts.append(process_row(x, temperature, top_k, top_p, keep_n=n))
+    return alts
 
 
 def final_pick(weights: np.ndarray, u: float):
@@ -157,6 +201,25 @@ def final_pick(weights: np.ndarray, u: float):
     v = int(above[0]) if above.size else int(np.flatnonzero(weights > 0)[-1])
     lo = cum[v - 1] if v > 0 else 0.0
     return v, min(abs(cum[v] - target), abs(target - lo))
+
+
+def pick_admissible(weights: np.ndarray, u: float, tol: float):
+    """Every token an inverse-CDF draw over ascending ids can return when
+    the point u * sum(weights) moves by up to ``tol`` (units of weights) and
+    stays at or above 0: the tokens v of positive weight whose interval
+    [cum[v-1], cum[v]) meets that band, and the last token of positive
+    weight when the band reaches the total (the draw's own fallback)."""
+    cum = np.cumsum(weights)
+    target = u * cum[-1]
+    lo_band, hi_band = max(0.0, target - tol), target + tol
+    out = set()
+    for v in range(len(weights)):
+        start = cum[v - 1] if v > 0 else 0.0
+        if weights[v] > 0 and start <= hi_band and cum[v] > lo_band:
+            out.add(v)
+    if hi_band >= cum[-1]:
+        out.add(int(np.flatnonzero(weights > 0)[-1]))
+    return out
 
 
 def pair_step(pt: Processed, pd: Processed, x: int, u: float, mode: int):
@@ -197,8 +260,11 @@ def decide_request(pt, pd, x, u, mode):
     else:
         if a < ell - 1:
             w = np.maximum(0.0, pt[a].p - pd[a].p)
-            if w.sum() == 0.0:
+            R = w.sum()
+            if R == 0.0:
                 w = pt[a].p
+            else:
+                margins.append(R)  # distance to the switch to p_t at R = 0
         else:
             w = pt[ell - 1].p
         final, mg = final_pick(w, float(u[ell - 1]))
@@ -257,6 +323,72 @@ def verify_request(t_rows, d_rows, x, u, temperature, top_k, top_p, mode,
         "topp_near_tie_t": [r.topp_margin < NEAR_TIE for r in pt],
         "topp_near_tie_d": [r.topp_margin < NEAR_TIE for r in pd],
     }
+
+
+def admissible_outcomes(t_rows, d_rows, x, u, temperature, top_k, top_p, mode,
+                        tol: float = NEAR_TIE):
+    """What the verify rules leave open for one request when every decision
+    may be flipped by a perturbation below ``tol`` (same arguments as
+    verify_request).
+
+    Each row may take any kept set of ``row_alternatives``.  Drafted
+    position j is decided when every pair of alternatives of its rows gives
+    the same accept outcome with margin |u_j - p_t/p_d| >= tol.  When every
+    test up to the first rejection (or the bonus row) is decided, the accept
+    length a is fixed and the final token lies in the union, over the
+    alternatives of row a's pair, of ``pick_admissible``; a residual mass
+    R with 0 < R < tol admits the draws from p_t as well.
+
+    Returns a dict: ``determined`` (the accept chain is fixed), ``accept_len``,
+    ``finals`` (set of admissible final tokens), ``conf`` (per drafted
+    position, the list of labels over the alternatives of its pair),
+    ``Z_t`` / ``Z_d`` (per row, the normalisers over its alternatives).
+    """
+    t_rows = np.atleast_2d(np.asarray(t_rows, dtype=np.float64))
+    ell = t_rows.shape[0]
+    V = t_rows.shape[1]
+    d_rows = np.asarray(d_rows, dtype=np.float64).reshape(ell - 1, V)
+    x = [int(v) for v in np.asarray(x).reshape(-1)]
+    T = temperature if temperature > 0 else 0.0
+    at = [row_alternatives(t_rows[j], T, top_k, top_p) for j in range(ell)]
+    ad = [row_alternatives(d_rows[j], T, top_k, top_p) for j in range(ell - 1)]
+    res = {"determined": True, "accept_len": None, "finals": set(),
+           "conf": [[conf_label(a, b) for a in at[j] for b in ad[j]] if T > 0 else []
+                    for j in range(ell - 1)],
+           "Z_t": [[r.Z for r in alts] for alts in at],
+           "Z_d": [[r.Z for r in alts] for alts in ad]}
+    a = ell - 1
+    for j in range(ell - 1):
+        outcomes = set()
+        for pt in at[j]:
+            for pd in ad[j]:
+                ok, mg = pair_step(pt, pd, x[j], float(u[j]), mode)
+                outcomes.add(bool(ok))
+                if mg < tol:
+                    outcomes.add(not ok)
+        if len(outcomes) > 1:
+            res["determined"] = False
+            return res
+        if not outcomes.pop():
+            a = j
+            break
+    res["accept_len"] = a
+    uf = float(u[ell - 1])
+    if mode == SV_GREEDY:
+        res["finals"] = {at[a][0].argmax}
+        return res
+    for pt in at[a]:
+        if a == ell - 1:
+            res["finals"] |= pick_admissible(pt.p, uf, tol)
+            continue
+        for pd in ad[a]:
+            w = np.maximum(0.0, pt.p - pd.p)
+            R = w.sum()
+            if R > 0.0:
+                res["finals"] |= pick_admissible(w, uf, tol)
+            if R < tol:
+                res["finals"] |= pick_admissible(pt.p, uf, tol)
+    return res
 
 
 def spec_verify_oracle(target, draft, draft_tokens, uniforms, verify_lens, row_offsets,

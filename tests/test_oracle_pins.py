@@ -44,6 +44,34 @@ def test_hand_derived_cases(case):
             np.testing.assert_allclose(out[key], np.array(case[key], float), rtol=0, atol=1e-12)
 
 
+@pytest.mark.parametrize("case", [c for c in json.load(open(GOLDEN))["cases"] if "margins" in c],
+                         ids=lambda c: c["name"])
+def test_hand_derived_margins(case):
+    """The decision margins, near-tie flag, fixed-or-open accept chain and the
+    admissible final tokens of hand-derived single-request cases (values in
+    the golden file, derived on paper)."""
+    mode = SV_SAMPLE if case["mode"] == "sample" else SV_GREEDY
+    t = _f32_rows(case["target"]).astype(np.float64)
+    d = (_f32_rows(case["draft"]).astype(np.float64) if case["draft"]
+         else np.zeros((0, t.shape[1])))
+    args = (t, d, case["draft_tokens"], np.array(case["uniforms"], np.float64),
+            case["temperature"], case["top_k"], case["top_p"], mode)
+    res = oracle.verify_request(*args)
+    finite = [m for m in res["margins"] if np.isfinite(m)]
+    assert finite == case["margins"]  # exact: every value is a sum of powers of two
+    assert res["near_tie"] == case["near_tie"][0]
+    adm = oracle.admissible_outcomes(*args)
+    assert adm["determined"] == case["determined"][0]
+    if adm["determined"]:
+        assert adm["accept_len"] == case["accept_len_expected"][0]
+        assert sorted(adm["finals"]) == case["finals"][0]
+    if "topp_sizes_t" in case:
+        got = [oracle.process_row(t[j], case["temperature"], case["top_k"], case["top_p"]).topp_sizes
+               for j in range(t.shape[0])]
+        assert got == case["topp_sizes_t"]
+        assert [sorted(z) for z in adm["Z_t"]] == [sorted(z) for z in case["Z_t"]]
+
+
 # --------------------------------------------------------------------------- helpers
 def brute_processed(x, T, top_k, top_p):
     """Filtered distribution by pairwise rank counting (no sort) + scipy softmax."""
@@ -301,3 +329,127 @@ def test_bf16_decode():
     assert got[:6].tolist() == [1.0, -1.0, 0.0, 0.0, np.inf, -np.inf]
     assert got[6] == 3.140625
     assert got[7] == 2.0 ** -133
+
+
+# --------------------------------------------------------------------------- near-tie sets
+def _draw_at(w, t):
+    """Inverse-CDF draw at the point t of the running sum, by a plain loop:
+    the first id whose running sum exceeds t, else the last positive id."""
+    run = 0.0
+    for v, wv in enumerate(w):
+        run += wv
+        if run > t:
+            return v
+    return max(v for v in range(len(w)) if w[v] > 0)
+
+
+def _probe_points(edges, lo, hi):
+    """Points of [lo, hi] that reach every piece of a step function with the
+    given breakpoints: both ends, each breakpoint inside, the float just above
+    it, and a dense grid."""
+    pts = [lo, hi] + list(np.linspace(lo, hi, 2001))
+    for e in edges:
+        if lo <= e <= hi:
+            pts += [e, np.nextafter(e, np.inf)]
+    return [p for p in pts if lo <= p <= hi]
+
+
+def test_pick_admissible_matches_pointwise_draws():
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        n = int(rng.integers(1, 12))
+        w = rng.uniform(0, 1, n) * 10.0 ** rng.integers(-7, 0, n)  # many tiny weights
+        w[rng.uniform(size=n) < 0.3] = 0.0
+        if w.sum() == 0:
+            w[int(rng.integers(0, n))] = 1e-3
+        cum = np.cumsum(w)
+        u = float(rng.uniform())
+        if rng.uniform() < 0.5:  # put u * total right next to an edge
+            u = min(0.999999, max(0.0, (cum[int(rng.integers(0, n))] + rng.normal(0, 3e-7)) / cum[-1]))
+        tol = float(rng.choice([1e-6, 1e-5, 1e-3]))
+        target = u * cum[-1]
+        lo, hi = max(0.0, target - tol), target + tol
+        want = {_draw_at(w, t) for t in _probe_points(cum, lo, hi)}
+        assert oracle.pick_admissible(w, u, tol) == want
+        assert oracle.final_pick(w, u)[0] in want
+
+
+def test_topp_sizes_match_pointwise_cuts():
+    rng = np.random.default_rng(12)
+    for _ in range(300):
+        n = int(rng.integers(1, 15))
+        p = rng.uniform(0, 1, n) * 10.0 ** rng.integers(-7, 0, n)
+        p = np.sort(p)[::-1] / p.sum()
+        cum = np.cumsum(p)
+        top_p = float(rng.uniform(0.05, 0.999))
+        if rng.uniform() < 0.5:  # a cut within a few 1e-7 of a cumulative value
+            top_p = float(np.clip(cum[int(rng.integers(0, n))] + rng.normal(0, 4e-7), 1e-3, 0.9999))
+        tol = float(rng.choice([1e-6, 1e-4]))
+
+        def cut(tp):  # shortest prefix reaching tp
+            for k in range(1, n + 1):
+                if cum[k - 1] >= tp:
+                    return k
+            return n
+        want = {cut(tp) for tp in _probe_points(cum, top_p - tol, top_p + tol)}
+        assert set(oracle.topp_sizes(cum, top_p, tol)) == want
+
+
+def test_admissible_outcomes_hold_every_perturbed_result():
+    """Soundness of the near-tie sets: moving each uniform and top_p by less
+    than the tolerance, the plain rules always land on an admissible outcome
+    (and on the unique one when the chain is fixed)."""
+    rng = np.random.default_rng(13)
+    tol = 1e-6
+    n_open = n_fixed = 0
+    for trial in range(150):
+        V, ell = int(rng.integers(3, 9)), int(rng.integers(1, 5))
+        t = rng.integers(-3, 4, size=(ell, V)).astype(float) * 0.5
+        d = t[: ell - 1] + rng.integers(-1, 2, size=(ell - 1, V)) * 0.5
+        T = float(rng.choice([1.0, 0.7]))
+        top_k, top_p = int(rng.choice([0, 4])), float(rng.choice([1.0, 0.9, 0.6]))
+        pt = [oracle.process_row(t[j], T, top_k, top_p) for j in range(ell)]
+        pd = [oracle.process_row(d[j], T, top_k, top_p) for j in range(ell - 1)]
+        x = [int(rng.choice(V, p=pd[j].p)) for j in range(ell - 1)]
+        u = rng.uniform(0, 1, ell)
+        if ell > 1 and rng.uniform() < 0.5:  # an accept test right at its ratio
+            r0 = pt[0].p[x[0]] / pd[0].p[x[0]]
+            if r0 < 1:
+                u[0] = r0 + rng.choice([-4e-7, 4e-7, 3e-6])
+        if rng.uniform() < 0.3 and top_p < 1:  # a top-p cut right at a boundary
+            top_p = float(np.cumsum(np.sort(pt[-1].p)[::-1])[0]) + float(rng.choice([-3e-7, 3e-7]))
+        adm = oracle.admissible_outcomes(t, d, x, u, T, top_k, top_p, SV_SAMPLE, tol)
+        n_fixed += adm["determined"]
+        n_open += not adm["determined"]
+        for _ in range(6):
+            du = rng.uniform(-0.45 * tol, 0.45 * tol, ell)
+            dp = float(rng.uniform(-0.45 * tol, 0.45 * tol)) if top_p < 1 else 0.0
+            up = np.clip(u + du, 0.0, 1.0 - 1e-12)
+            out = oracle.verify_request(t, d, x, up, T, top_k, min(1.0, top_p + dp), SV_SAMPLE)
+            if adm["determined"]:
+                assert out["accept_len"] == adm["accept_len"]
+                assert int(out["tokens"][out["accept_len"]]) in adm["finals"]
+    assert n_open > 0 and n_fixed > 50
+
+
+def test_small_residual_mass_is_a_near_tie():
+    """At a rejection, the choice between the residual and p_t switches at
+    R = 0: R is that choice's margin.  Rows [0, 0] (target) and [delta, 0]
+    (draft), x = 0: p_d(0) > p_t(0) = 1/2 and ratio = 1/2 (1 + e^-delta)
+    ~ 1 - delta/2, so u = 1 - 2^-24 rejects with margin ~ delta/2 > 1e-6 for
+    both deltas below; R = p_t(1) - p_d(1) = tanh(delta/2) / 2 ~ delta/4.
+    The residual sits on id 1 alone; p_t with u = 1/4 would draw id 0."""
+    for delta, finals in ((1e-5, {1}), (3e-6, {0, 1})):
+        delta = float(np.float32(delta))
+        t = np.array([[0.0, 0.0], [0.0, 0.0]])
+        d = np.array([[delta, 0.0]])
+        u = np.array([1 - 2.0 ** -24, 0.25])
+        out = oracle.verify_request(t, d, [0], u, 1.0, 0, 1.0, SV_SAMPLE)
+        assert out["accept_len"] == 0 and out["tokens"].tolist() == [1, -1]
+        R = math.tanh(delta / 2) / 2
+        # fp64 cancellation in p_t - p_d: about 1e-16 absolute
+        assert any(abs(m - R) <= 1e-9 * R for m in out["margins"])
+        assert out["margins"][0] > 1e-6  # the accept test itself is clear
+        adm = oracle.admissible_outcomes(t, d, [0], u, 1.0, 0, 1.0, SV_SAMPLE)
+        assert adm["determined"] and adm["accept_len"] == 0
+        assert adm["finals"] == finals  # R < 1e-6 admits the p_t draw too

@@ -97,3 +97,17 @@ def test_sps_table_bounds_the_batch():
     assert res["lens"].sum() == 5
     with pytest.raises(ValueError):
         oracle.schedule_prefix(conf, np.full(3, 1.0))  # no entry for B = 3
+
+
+@pytest.mark.parametrize("sign,lens,added", [(+1, [2], 1), (-1, [1], 0)])
+def test_near_tied_theta_margin(sign, lens, added):
+    """Hand case: one request, c = 1/2, SPS = [0, 3/2, 1 + s 2^-36].  Start:
+    tau = 1, Theta = 3/2.  The candidate S = 1/2 gives tau = 3/2 and
+    Theta_next = 3/2 (1 + s 2^-36), exact in float64: it is added only when
+    s = +1, and the recorded margin is the relative gap 2^-36 (about 1.5e-11)
+    either way."""
+    sps = np.array([0.0, 1.5, 1.0 + sign * 2.0 ** -36])
+    res = oracle.schedule_prefix(np.array([[0.5]]), sps)
+    assert res["lens"].tolist() == lens and res["added"] == added
+    assert res["margin"] == 2.0 ** -36
+    assert res["theta"] == (1.5 * (1.0 + 2.0 ** -36) if sign > 0 else 1.5)
