@@ -23,10 +23,13 @@
  *     page, section "这份权重是什么");
  *   - temperature, top_k, top_p processing of both models (DSpine page,
  *     section "加速效果": T 1.0, top_p 0.95, top_k 20).
- * Readings the pages leave open (filter order temperature -> top-k ->
- * renormalise -> top-p -> renormalise; ties broken by (value desc, id asc);
- * inverse CDF over ascending ids with a strict ">"; one uniform per target
- * row) are the same as the CPU oracle's and are listed in the design doc.
+ * Where the pages leave a step open, this library reads it as follows (the
+ * CPU oracle reads it the same way): filter order temperature -> top-k ->
+ * renormalise -> top-p (the shortest prefix reaching top_p) -> renormalise;
+ * ties broken by (value desc, id asc), -0 and +0 being one value; inverse
+ * CDF over ascending ids with a strict ">"; one uniform per target row; a
+ * residual mass max(0, p_t - p_d) that is zero up to fp32 rounding (at most
+ * 2^-21) falls back to p_t.
  *
  * Layout.  B requests; request r owns l_r target rows (1 <= l_r <= max_len):
  * rows row_offsets[r] .. row_offsets[r] + l_r - 1 of target_logits, where
@@ -259,6 +262,34 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
 #define SV_SCHEDULE_MAX_CANDIDATES 8192
 int spec_verify_schedule(const float* conf, int32_t B, int32_t K, const double* sps,
                          int32_t n_sps, int32_t* out_lens, double* out_theta, void* stream);
+
+/*
+ * Tuning and testing hook (the pages have no counterpart): sets one
+ * process-wide knob of the rows kernel for every later call; value < 0
+ * restores its default.  The defaults are the shipped configuration; the
+ * library reads no environment variable.
+ *   SV_TUNE_SLICE        target slice length in elements (0 or default: 22000
+ *                        bytes' worth), up to 2^24
+ *   SV_TUNE_STAGES       most shared-memory stages, 4..6
+ *   SV_TUNE_WARPS        consumer warps, 16 or 24
+ *   SV_TUNE_PASS1_WARPS  consumer warps on pass 1 when labels are on, 0 (half)
+ *                        .. 23
+ *   SV_TUNE_POLL_NS      sleep between polls of another CTA's words, 0..10000
+ *   SV_TUNE_XWAIT_NS     limit of a wait on words that other CTAs of the
+ *                        same launch publish, 0..200000000 (default 200 ms);
+ *                        a wait that reaches it gives up, the call raises
+ *                        SV_DEVERR_TIMEOUT and its outputs are unspecified
+ *                        (waits on a CTA's own copies keep their own limit).
+ * Host only; takes effect on the next call.  Returns SV_OK or SV_ERR_ARG
+ * (unknown knob, value out of range).
+ */
+#define SV_TUNE_SLICE 0
+#define SV_TUNE_STAGES 1
+#define SV_TUNE_WARPS 2
+#define SV_TUNE_PASS1_WARPS 3
+#define SV_TUNE_POLL_NS 4
+#define SV_TUNE_XWAIT_NS 5
+int spec_verify_set_tuning(int32_t knob, int64_t value);
 
 /* Static text for a status code (host). */
 const char* spec_verify_status_string(int status);

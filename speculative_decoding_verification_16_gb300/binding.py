@@ -53,10 +53,24 @@ _lib.spec_verify_schedule.restype = ctypes.c_int
 SV_SCHEDULE_MAX_CANDIDATES = 8192
 
 
+SV_TUNE_SLICE, SV_TUNE_STAGES, SV_TUNE_WARPS, SV_TUNE_PASS1_WARPS = 0, 1, 2, 3
+SV_TUNE_POLL_NS, SV_TUNE_XWAIT_NS = 4, 5
+_lib.spec_verify_set_tuning.argtypes = [_i32, ctypes.c_int64]
+_lib.spec_verify_set_tuning.restype = ctypes.c_int
+
+
 class SpecVerifyError(RuntimeError):
     def __init__(self, status: int):
         super().__init__(f"spec_verify failed ({status}): {spec_verify_status_string(status)}")
         self.status = status
+
+
+def spec_verify_set_tuning(knob: int, value: int) -> None:
+    """Process-wide tuning knob of the rows kernel (tests and sweeps);
+    ``value`` < 0 restores the default."""
+    rc = _lib.spec_verify_set_tuning(int(knob), int(value))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc)
 
 
 def spec_verify_status_string(status: int) -> str:
@@ -114,14 +128,20 @@ def alloc_workspace(B: int, n_target_rows: int, device) -> torch.Tensor:
 
 class PreparedCall:
     """A call with its arguments marshalled once; ``__call__`` re-issues it
-    (used by timing loops, where per-call marshalling would dominate)."""
+    (used by timing loops, where per-call marshalling would dominate).  The
+    call runs with the tensors' device current, as the C ABI requires."""
 
-    def __init__(self, fn, args):
+    def __init__(self, fn, args, device):
         self._fn = fn
         self._args = args
+        self._device = device
 
     def __call__(self):
-        rc = self._fn(*self._args)
+        if torch.cuda.current_device() != self._device:
+            with torch.cuda.device(self._device):
+                rc = self._fn(*self._args)
+        else:
+            rc = self._fn(*self._args)
         if rc != SV_OK:
             raise SpecVerifyError(rc)
 
@@ -144,7 +164,7 @@ def prepare(entry: str, target_logits, draft_logits, draft_tokens, uniforms, ver
             _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.conf), _ptr(out.row_stats),
             _ptr(out.dev_error), _ptr(workspace), _sz(workspace.numel()),
             ctypes.c_void_p(stream.cuda_stream))
-    return PreparedCall(getattr(_lib, entry), args)
+    return PreparedCall(getattr(_lib, entry), args, target_logits.device.index)
 
 
 def spec_verify(target_logits, draft_logits, draft_tokens, uniforms, verify_lens, row_offsets,
@@ -186,7 +206,20 @@ def spec_verify_static(target_logits, draft_logits, draft_tokens, uniforms, veri
     n_target_rows, V = target_logits.shape
     if stream is None:
         stream = torch.cuda.current_stream(target_logits.device)
-    rc = _lib.spec_verify_static(
+    out.dev_error.zero_()  # this call's flags only (a kernel on the stream, no allocation)
+    # the library picks the static array of the current device
+    with torch.cuda.device(target_logits.device):
+        rc = _call_static(target_logits, draft_logits, draft_tokens, uniforms, verify_lens,
+                          row_offsets, B, V, n_target_rows, max_len, temperature, top_k, top_p,
+                          mode, out, stream)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc)
+    return out
+
+
+def _call_static(target_logits, draft_logits, draft_tokens, uniforms, verify_lens, row_offsets,
+                 B, V, n_target_rows, max_len, temperature, top_k, top_p, mode, out, stream):
+    return _lib.spec_verify_static(
         _ptr(target_logits), _ptr(draft_logits) if draft_logits.numel() else None,
         _ptr(draft_tokens) if draft_tokens.numel() else None, _ptr(uniforms),
         _ptr(verify_lens), _ptr(row_offsets),
@@ -195,9 +228,6 @@ def spec_verify_static(target_logits, draft_logits, draft_tokens, uniforms, veri
         _i32(mode),
         _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.conf), _ptr(out.row_stats),
         _ptr(out.dev_error), ctypes.c_void_p(stream.cuda_stream))
-    if rc != SV_OK:
-        raise SpecVerifyError(rc)
-    return out
 
 
 def verify_workload(w, *, want_conf=True, want_stats=False, **kw) -> Outputs:

@@ -8,7 +8,6 @@
 
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
 #include <algorithm>
 #include <atomic>
 #include <mutex>
@@ -36,9 +35,23 @@ struct DeviceCache {
 std::mutex g_mu;
 DeviceCache g_dev[kMaxDevices];
 
-int env_int(const char* name, int dflt) {
-  const char* v = std::getenv(name);
-  return v ? std::atoi(v) : dflt;
+// Process-wide tuning of the rows kernel.  The defaults are the shipped
+// configuration; only spec_verify_set_tuning changes them (tests and
+// sweeps), so no call reads the environment.
+struct Tuning {
+  int slice = 0;            // target slice length in elements; 0: 22000 bytes' worth
+  int stages = kMaxStages;  // most shared-memory stages
+  int warps = 16;           // consumer warps (16 or 24)
+  int pass1_warps = 0;      // consumer warps on pass 1 with labels on; 0: half
+  int poll_ns = 128;        // sleep between polls of another CTA's words
+  int64_t xwait_ns = static_cast<int64_t>(kWaitLimitNs);  // limit of a wait on other CTAs
+};
+std::mutex g_tune_mu;
+Tuning g_tune;
+
+Tuning tuning() {
+  std::lock_guard<std::mutex> lock(g_tune_mu);
+  return g_tune;
 }
 
 int device_info(DeviceCache* out) {
@@ -74,8 +87,8 @@ int filter_k(int V, int top_k, float top_p) {
 
 // Geometry of the rows kernel: a row is cut into S <= kMaxSlices slices of
 // L elements (L a multiple of the 16-byte vector; about 11000 bf16 / 5500
-// fp32 elements by default, SPEC_VERIFY_SLICE overrides) and as many stages
-// (kMinStages .. kMaxStages, SPEC_VERIFY_STAGES caps) as the shared memory
+// fp32 elements by default, SV_TUNE_SLICE overrides) and as many stages
+// (kMinStages .. kMaxStages, SV_TUNE_STAGES caps) as the shared memory
 // allows next to the row_offsets copy (B + 1 entries when they fit).
 struct RowsGeom {
   int L, S, stages, smem, offs_smem;
@@ -83,13 +96,14 @@ struct RowsGeom {
 
 int rows_geometry(int V, int B, int es, const DeviceCache& dc, RowsGeom* g) {
   const int vec = 16 / es;
-  const int target = env_int("SPEC_VERIFY_SLICE", 22000 / es);
+  const Tuning tu = tuning();
+  const int target = tu.slice > 0 ? tu.slice : 22000 / es;
   int S = std::max(1, (V + target - 1) / target);
   S = std::min(S, kMaxSlices);
   const int L = round_up((V + S - 1) / S, vec);
   S = (V + L - 1) / L;  // no empty trailing slice
   const int offs = B + 1 <= kMaxSmemOffsets ? round_up((B + 1) * 4, 128) : 0;
-  const int max_stages = std::min(kMaxStages, env_int("SPEC_VERIFY_STAGES", kMaxStages));
+  const int max_stages = std::min(kMaxStages, tu.stages);
   for (int ns = max_stages; ns >= kMinStages; --ns) {
     const int smem = kRowsHdrBytes + ns * 2 * rowbuf_bytes(L, es) + offs;
     if (smem <= dc.max_smem_optin) {
@@ -361,7 +375,9 @@ int run_rows(const Args& a, bool fuse) {
   P.nstages = geo.stages;
   P.tag = next_tag();
   P.offs_smem = geo.offs_smem;
-  P.poll_ns = std::max(0, std::min(10000, env_int("SPEC_VERIFY_POLL_NS", 128)));
+  const Tuning tu = tuning();
+  P.poll_ns = tu.poll_ns;
+  P.xwait_ns = static_cast<uint64_t>(tu.xwait_ns);
   P.fuse = fuse ? 1 : 0;
   const int smem = geo.smem;
   // z is needed for sampling, labels and statistics; the exact max / argmax
@@ -372,9 +388,9 @@ int run_rows(const Args& a, bool fuse) {
   const bool need_conf = a.out_conf != nullptr || a.mode == SV_SAMPLE;
   const bool track = a.mode == SV_GREEDY || a.out_row_stats != nullptr;
   // consumer warps (16 or 24) and, with labels, how many of them run pass 1
-  // (SPEC_VERIFY_WARPS, SPEC_VERIFY_PASS1_WARPS)
-  const int ncw = env_int("SPEC_VERIFY_WARPS", 16) >= 24 ? 24 : 16;
-  P.nw1 = std::max(1, std::min(ncw - 1, env_int("SPEC_VERIFY_PASS1_WARPS", ncw / 2)));
+  // (SV_TUNE_WARPS, SV_TUNE_PASS1_WARPS)
+  const int ncw = tu.warps >= 24 ? 24 : 16;
+  P.nw1 = std::max(1, std::min(ncw - 1, tu.pass1_warps > 0 ? tu.pass1_warps : ncw / 2));
   if (es == 2)
     return ncw == 24 ? launch_rows<2, 24>(P, smem, dc, need_z, need_conf, track, st)
                      : launch_rows<2, 16>(P, smem, dc, need_z, need_conf, track, st);
@@ -524,13 +540,15 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
   if (n_target_rows > SV_STATIC_MAX_ROWS ||
       spec_verify_workspace_size(B, n_target_rows) > sv::kStaticBytes)
     return SV_ERR_TOO_LARGE;
-  void* ws = nullptr;
-  int rc = sv::static_workspace(&ws, static_cast<cudaStream_t>(stream));
-  if (rc != SV_OK) return rc;
+  // the host checks run first, against a stand-in for the array (aligned,
+  // non-null, never dereferenced): a call with bad arguments enqueues nothing,
+  // not even the first call's clear of the array
   const size_t workspace_bytes = sv::kStaticBytes;
-  void* workspace = ws;
+  void* workspace = reinterpret_cast<void*>(static_cast<uintptr_t>(256));
   SV_ARGS_PACK;
-  rc = sv::check_args(a);
+  int rc = sv::check_args(a);
+  if (rc != SV_OK) return rc;
+  rc = sv::static_workspace(&a.workspace, static_cast<cudaStream_t>(stream));
   return rc != SV_OK ? rc : sv::run_call(a);
 }
 
@@ -568,6 +586,41 @@ const char* spec_verify_status_string(int status) {
       return "problem larger than the static scratch of spec_verify_static "
              "(more than SV_STATIC_MAX_ROWS target rows)";
     default: return "unknown status";
+  }
+}
+
+int spec_verify_set_tuning(int32_t knob, int64_t value) {
+  std::lock_guard<std::mutex> lock(sv::g_tune_mu);
+  sv::Tuning& t = sv::g_tune;
+  const sv::Tuning d{};
+  const bool dflt = value < 0;
+  switch (knob) {
+    case SV_TUNE_SLICE:
+      if (!dflt && value > (1 << 24)) return SV_ERR_ARG;
+      t.slice = dflt ? d.slice : static_cast<int>(value);
+      return SV_OK;
+    case SV_TUNE_STAGES:
+      if (!dflt && (value < sv::kMinStages || value > sv::kMaxStages)) return SV_ERR_ARG;
+      t.stages = dflt ? d.stages : static_cast<int>(value);
+      return SV_OK;
+    case SV_TUNE_WARPS:
+      if (!dflt && value != 16 && value != 24) return SV_ERR_ARG;
+      t.warps = dflt ? d.warps : static_cast<int>(value);
+      return SV_OK;
+    case SV_TUNE_PASS1_WARPS:
+      if (!dflt && value > 23) return SV_ERR_ARG;
+      t.pass1_warps = dflt ? d.pass1_warps : static_cast<int>(value);
+      return SV_OK;
+    case SV_TUNE_POLL_NS:
+      if (!dflt && value > 10000) return SV_ERR_ARG;
+      t.poll_ns = dflt ? d.poll_ns : static_cast<int>(value);
+      return SV_OK;
+    case SV_TUNE_XWAIT_NS:
+      if (!dflt && value > static_cast<int64_t>(sv::kWaitLimitNs)) return SV_ERR_ARG;
+      t.xwait_ns = dflt ? d.xwait_ns : value;
+      return SV_OK;
+    default:
+      return SV_ERR_ARG;
   }
 }
 

@@ -86,6 +86,7 @@ struct Params {
   int32_t offs_smem; // row_offsets copied into shared memory (B + 1 <= kMaxSmemOffsets)
   int32_t nw1;       // rows kernel, labels on: consumer warps running pass 1
   int32_t poll_ns;   // rows kernel: gatherer sleep between polls
+  uint64_t xwait_ns; // limit of a wait on words published by other CTAs
   int32_t fuse;      // rows kernel: finish the requests in its tail (no finalize launch)
 };
 

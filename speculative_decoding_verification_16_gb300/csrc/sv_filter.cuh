@@ -50,8 +50,11 @@ struct FiltRow {
 };
 static_assert(sizeof(FiltRow) == 544, "FiltRow layout");
 
+// Order-preserving key of a logit: a larger key is a larger value.  -0 and
+// +0 are one value (ties among them go by token id), so -0 is keyed as +0.
 __device__ __forceinline__ uint32_t order_key(float x) {
-  const uint32_t u = __float_as_uint(x);
+  uint32_t u = __float_as_uint(x);
+  u = u == 0x80000000u ? 0u : u;
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 

@@ -20,20 +20,24 @@
 // over: running sums in (thread, element) order are sums in ascending token
 // id.  fp32 slice masses differ from the exact ones by a few 1e-7 in
 // probability, inside the near-tie margin the oracle reports.  A residual
-// mass below kZeroResidual counts as zero: the draw then uses p_t, as the
-// exact method does when max(0, p_t - p_d) vanishes.
+// mass at or below kZeroResidual counts as zero: the draw then uses p_t, as
+// the exact method does when max(0, p_t - p_d) vanishes.
 #pragma once
 
 #include "sv_common.cuh"
 
 namespace sv {
 
-// A residual mass sum max(0, p_t - p_d) below this is taken for zero (the
-// draw then uses p_t): the fp32 slice masses of two equal distributions
-// differ by rounding of order 1e-7, and a rejection with so little residual
-// mass happens with probability below it (it needs p_d(x) = 0 or p_t within
-// this of p_d everywhere).
-constexpr float kZeroResidual = 7.62939453125e-06f;  // 2^-17
+// A residual mass sum max(0, p_t - p_d) at or below this is taken for zero
+// (the draw then uses p_t).  The fp32 slice masses of two equal
+// distributions differ by rounding of order 1e-7, so an exact zero is not
+// seen as one.  The cutoff sits below the 1e-6 near-tie margin: a residual
+// mass of 1e-6 or more is always drawn from (its fp32 estimate is off by far
+// less than the 5e-7 between the two), and a smaller one is a near tie of
+// the choice between the residual and p_t.  A slice whose mass was rounding
+// only is found and dropped by the draw itself (its recomputed weights are
+// all zero).
+constexpr float kZeroResidual = 4.76837158203125e-07f;  // 2^-21
 
 constexpr int kDrawThreads = 512;  // threads per CTA of the draw kernel
 constexpr int kDrawWarps = kDrawThreads / 32;
@@ -260,7 +264,7 @@ __device__ __forceinline__ bool finish_request(const Params& P, int32_t r, const
     if (wait_ready && (v & 0xffffffff00000000ull) != tagw) {
       const uint64_t t0 = globaltimer_ns();
       while (((v = ld_cg_u64(wp)) & 0xffffffff00000000ull) != tagw) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 >= P.xwait_ns) {
           stale = true;
           break;
         }

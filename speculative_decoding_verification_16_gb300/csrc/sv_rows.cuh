@@ -583,7 +583,8 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
   }
   __syncthreads();
 
-  bool timeout = false;
+  bool timeout = false;   // a wait on this CTA's own barriers gave up
+  bool xtimeout = false;  // a wait on other CTAs' published words gave up
   if (warp < NCW) {
     // =============================== consumer warps
     // Labels on: warps [0, NW1) run pass 1, warps [NW1, NCW) pass 2, each
@@ -748,7 +749,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
       const uint64_t* row_parts = parts + static_cast<size_t>(info.g) * kMaxSlices * kPartWords;
       const bool mine = lane < P.nslices;
       const uint64_t* src = row_parts + (mine ? lane : 0) * kPartWords;
-      uint32_t wv[R_NWORDS];
+      uint32_t wv[R_NWORDS] = {};
       auto full_read = [&]() {
         bool ok = true;
         if (mine) {
@@ -767,8 +768,11 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         const bool seen = !mine || (ld_relaxed_u64(src + R_BAD) & 0xffffffff00000000ull) == tagw;
         if (__all_sync(0xffffffffu, seen)) done = __all_sync(0xffffffffu, full_read());
         if (!done) {
-          if (timeout || globaltimer_ns() - t0 > kWaitLimitNs) {
-            timeout = true;
+          // a wait on other CTAs gives up after P.xwait_ns: the row's
+          // statistics are then wrong and the call reports a timeout, but
+          // this CTA's own pipeline (every wait below) runs on unchanged
+          if (xtimeout || globaltimer_ns() - t0 >= P.xwait_ns) {
+            xtimeout = true;
             break;
           }
           if (P.poll_ns > 0) __nanosleep(P.poll_ns);
@@ -789,7 +793,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         hasx = wv[R_HASX] != 0;
       }
       rstat_warp_reduce2<TRACK>(gt, gdr);
-      flags = __reduce_or_sync(0xffffffffu, flags) | (timeout ? SV_DEVERR_TIMEOUT : 0);
+      flags = __reduce_or_sync(0xffffffffu, flags) | (timeout || xtimeout ? SV_DEVERR_TIMEOUT : 0);
       const unsigned xl = __ballot_sync(0xffffffffu, hasx);
       if (xl) {
         xt = __shfl_sync(0xffffffffu, xt, __ffs(xl) - 1);
@@ -852,13 +856,14 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
       if (lane == 0) mbar_arrive(sm.empty(s));
     }
   }
-  if (timeout && lane == 0) raise_error(P, SV_DEVERR_TIMEOUT);
+  if ((timeout || xtimeout) && lane == 0) raise_error(P, SV_DEVERR_TIMEOUT);
   if (!P.fuse) return;
   // ---- tail: every role has left its loop and every copy has been consumed,
   //      so stage 0's buffers are free; this CTA finishes requests blockIdx.x,
   //      blockIdx.x + gridDim.x, ... as soon as their rows are done elsewhere
-  //      (skipped after a timeout: the stages may still be in use)
-  if (__syncthreads_or(timeout ? 1 : 0)) return;
+  //      (skipped after a timeout: the stages may still be in use, or the
+  //      statistics are wrong)
+  if (__syncthreads_or(timeout || xtimeout ? 1 : 0)) return;
   const FinishSmem fs{reinterpret_cast<DrawSel*>(smem_raw + kOffTail),
                       reinterpret_cast<float*>(smem_raw + kOffTail + 64),
                       reinterpret_cast<uint32_t*>(smem_raw + kOffPart),  // free after the loops
