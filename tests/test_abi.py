@@ -140,3 +140,31 @@ def test_schedule_rejects_bad_host_arguments(lib):
     assert f(p, 4, 3, q, 10, None, None, None) == -1         # out_lens missing
     assert f(p, 4, 3, q + 4, 10, p, None, None) == -1        # sps not 8-byte aligned
     assert f(p, 1000, 9, q, 10000, p, None, None) == -4      # above SV_SCHEDULE_MAX_CANDIDATES
+
+
+def test_static_entry_checks_arguments_before_anything_else(lib):
+    """A first call of the no-allocation entry point with a bad argument
+    returns SV_ERR_ARG from its host checks, before it looks up its array or
+    enqueues its clear (no device call happens: this runs without a GPU)."""
+    fake = 1 << 20
+    f = lib.spec_verify_static
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_float
+    f.argtypes = [vp] * 6 + [i32] * 4 + [i32, f32, i32, f32, i32] + [vp] * 5 + [vp]
+    f.restype = ctypes.c_int
+    assert f(fake, fake, fake, fake, fake, fake, 2, 1000, 8, 4, 0, 0.0, 0, 1.0, 1,
+             fake, fake, fake, None, None, None) == -1  # sampling with T = 0
+    assert f(None, fake, fake, fake, fake, fake, 2, 1000, 8, 4, 0, 1.0, 0, 1.0, 1,
+             fake, fake, fake, None, None, None) == -1  # no target logits
+
+
+def test_set_tuning_checks_knobs(lib):
+    f = lib.spec_verify_set_tuning
+    f.argtypes = [ctypes.c_int32, ctypes.c_int64]
+    f.restype = ctypes.c_int
+    assert f(99, 1) == -1              # unknown knob
+    assert f(1, 3) == -1               # fewer stages than the pipeline allows
+    assert f(2, 20) == -1              # consumer warps are 16 or 24
+    assert f(5, 10 ** 12) == -1        # cross-CTA wait limit above 200 ms
+    for knob in range(6):              # defaults restore
+        assert f(knob, -1) == 0
+    assert f(4, 256) == 0 and f(4, -1) == 0

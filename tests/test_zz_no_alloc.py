@@ -25,18 +25,21 @@ def _host(o):
             int(o.dev_error.item()))
 
 
-@pytest.mark.parametrize("idx,mode,B", [
-    (0, W.SAMPLE, None),
-    (2, W.SAMPLE, None),       # conc32: B=32, block 16, V=151,936 bf16
-    (2, W.GREEDY, None),
-    (3, W.SAMPLE, 200),        # ragged lengths, V=129,280
+@pytest.mark.parametrize("idx,mode,B,top_k,top_p", [
+    (0, W.SAMPLE, None, None, None),
+    (2, W.SAMPLE, None, None, None),   # conc32: B=32, block 16, V=151,936 bf16
+    (2, W.GREEDY, None, None, None),
+    (3, W.SAMPLE, 200, None, None),    # ragged lengths, V=129,280
+    (4, W.SAMPLE, 8, None, None),      # top_k 20, top_p 0.95: the small kept-set path
+    (2, W.SAMPLE, 8, 0, 0.95),         # top-p over the whole row: the general path
 ])
-def test_static_entry_matches_workspace_entry(cuda_lib, idx, mode, B):
+def test_static_entry_matches_workspace_entry(cuda_lib, idx, mode, B, top_k, top_p):
     spec = W.WORKLOADS[idx]
     w = W.make_workload(spec, mode, seed=31, device=DEV, **({} if B is None else {"B": B}))
     assert w.target.shape[0] <= cuda_lib.SV_STATIC_MAX_ROWS
-    kw = dict(max_len=spec.max_len, temperature=spec.temperature, top_k=spec.top_k,
-              top_p=spec.top_p, mode=mode)
+    kw = dict(max_len=spec.max_len, temperature=spec.temperature,
+              top_k=spec.top_k if top_k is None else top_k,
+              top_p=spec.top_p if top_p is None else top_p, mode=mode)
     ref = cuda_lib.spec_verify(w.target, w.draft, w.draft_tokens, w.uniforms, w.verify_lens,
                                w.row_offsets, want_conf=True, want_stats=True, **kw)
     torch.cuda.synchronize()
