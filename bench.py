@@ -22,6 +22,13 @@ collective on the data path), time = max over ranks.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload I] [--mode sample|greedy]
 
+After the headline line's own workload, the same line carries
+``per_workload``: every one of the five synthetic workloads in each of its
+modes, timed the same way (inputs larger than L2 alternate; smaller ones
+get an L2 flush before each step, outside the step's events), with the
+dominant kernel's HBM fraction and the oracle's check of one call on a
+sample of requests (near ties, open accept chains, mismatches).
+
 --component schedule prints one line for the DSpark prefix scheduler instead
 (spec_verify_schedule on a pool of 256 requests x 15 positions whose
 confidences are the verify step's own labels on the ragged workload; the
@@ -68,6 +75,8 @@ def parse():
                          "(small cases for profiling; the timed default keeps B)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true",
+                    help="skip the per-workload lines (all five workloads in their modes)")
     ap.add_argument("--component", choices=("verify", "schedule"), default="verify")
     ap.add_argument("--top-k", type=int, default=None, help="override the workload's top_k")
     ap.add_argument("--top-p", type=float, default=None, help="override the workload's top_p")
@@ -166,25 +175,36 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+# Source files that make up each kernel whose DRAM traffic is recorded under
+# profiles/ (the kernel's own header, the headers it includes, the launch code).
+KERNEL_SOURCES = {
+    "rows_kernel": ["csrc/sv_rows.cuh", "csrc/sv_finalize.cuh", "csrc/sv_common.cuh",
+                    "csrc/sv_ptx.cuh", "csrc/spec_verify.cu", "../include/spec_verify.h"],
+    "filter_rows_kernel": ["csrc/sv_filter.cuh", "csrc/sv_common.cuh", "csrc/sv_ptx.cuh",
+                           "csrc/spec_verify.cu", "../include/spec_verify.h"],
+    "gfilter_rows_kernel": ["csrc/sv_gfilter.cuh", "csrc/sv_filter.cuh", "csrc/sv_common.cuh",
+                            "csrc/sv_ptx.cuh", "csrc/spec_verify.cu", "../include/spec_verify.h"],
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
-    csrc = os.path.join(PKG, "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(PKG, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload_name):
-    """DRAM bytes per launch of the rows kernel from the committed ncu summary,
-    or None when the kernel sources changed since it was captured."""
-    path = os.path.join(ROOT, "profiles", "rows_kernel_traffic.json")
+def recorded_traffic(kernel, workload_name):
+    """DRAM bytes per launch of ``kernel`` on the workload from the committed
+    ncu summary, or None when that kernel's sources changed since the
+    capture."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         rec = json.load(open(path))
     except (OSError, ValueError):
         return None
-    ent = rec.get(workload_name)
-    if not ent or ent.get("source_sha256") != kernel_source_hash():
+    ent = rec.get(f"{kernel}/{workload_name}")
+    if not ent or ent.get("source_sha256") != kernel_source_hash(kernel):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -223,6 +243,54 @@ def oracle_rate(w, spec, mode, budget_s, ell_cap=None, start=0, top_k=None, top_
         pos += ell - 1
         nreq += 1
     return pos / secs, pos, secs, nreq
+
+
+def oracle_check(w, out, spec, mode, top_k, top_p, budget_s, seed=0):
+    """The fp64 oracle on a seeded sample of the workload's requests (whole
+    requests, at least one, until ``budget_s`` of oracle time): its rate, and
+    how the library's outputs of one call compare with it -- requests with a
+    decision margin below 1e-6 (near ties), requests whose accept chain such
+    a margin leaves open (not compared), final tokens checked against a set
+    of admissible tokens, and mismatches (must be 0)."""
+    import numpy as np
+
+    import oracle
+    lens = w.verify_lens.cpu().numpy()
+    offs = w.row_offsets.cpu().numpy()
+    toks = out.tokens.cpu().numpy()
+    acc = out.accept_len.cpu().numpy()
+    dt = W.dtype_name(w.target)
+    order = np.random.default_rng(seed).permutation(w.B)
+    c = {"requests": 0, "positions": 0, "near_tie": 0, "open": 0, "final_sets": 0,
+         "mismatches": 0}
+    secs = 0.0
+    for r in order:
+        if c["requests"] and secs >= budget_s:
+            break
+        off, ell = int(offs[r]), int(lens[r])
+        doff = off - r
+        t = oracle.decode_logits(W.bits_of(w.target[off:off + ell]), dt)
+        d = oracle.decode_logits(W.bits_of(w.draft[doff:doff + ell - 1]), dt).reshape(ell - 1, w.V)
+        x = w.draft_tokens[doff:doff + ell - 1].cpu().numpy()
+        u = w.uniforms[off:off + ell].double().cpu().numpy()
+        t0 = time.perf_counter()
+        ex = oracle.verify_request(t, d, x, u, spec.temperature, top_k, top_p, mode)
+        secs += time.perf_counter() - t0
+        adm = oracle.admissible_outcomes(t, d, x, u, spec.temperature, top_k, top_p, mode)
+        c["requests"] += 1
+        c["positions"] += ell - 1
+        c["near_tie"] += bool(ex["near_tie"])
+        if not adm["determined"]:
+            c["open"] += 1
+            continue
+        a = adm["accept_len"]
+        got = toks[off:off + ell].tolist()
+        ok = (acc[r] == a and got[:a] == ex["tokens"][:a].tolist() and got[a] in adm["finals"]
+              and all(v == -1 for v in got[a + 1:]))
+        c["mismatches"] += not ok
+        c["final_sets"] += len(adm["finals"]) > 1
+    rate = c["positions"] / secs if secs > 0 else None
+    return c, rate, secs
 
 
 def run_reference(args, world, rank):
@@ -264,6 +332,117 @@ def run_reference(args, world, rank):
 
 
 # --------------------------------------------------------------------- ours
+L2_BYTES = 129 * 1024 * 1024
+
+
+def row_kernel_name(top_k, top_p, V):
+    """The launch that streams the logits (the dominant kernel)."""
+    if not ((0 < top_k < V) or top_p < 1.0):
+        return "rows_kernel"
+    return "filter_rows_kernel" if 0 < top_k <= 64 else "gfilter_rows_kernel"
+
+
+class Prepared:
+    """Input sets of one workload on the device with their marshalled calls:
+    unfiltered, one launch per step (the rows kernel finishes the requests in
+    its tail); filtered, the row kernel then the request kernel."""
+
+    def __init__(self, L, spec, mode, dev, stream, seed, top_k, top_p, requests=0, n_sets=2):
+        kw = {"B": requests} if requests > 0 else {}
+        self.sets = [W.make_workload(spec, mode, seed=seed + 100 * i, device=dev, **kw)
+                     for i in range(n_sets)]
+        w = self.sets[0]
+        if any(s.n_target_rows != w.n_target_rows for s in self.sets):
+            self.sets = self.sets[:1]  # ragged sets of other lengths: keep one
+        self.w = w
+        self.filtered = (0 < top_k < w.V) or top_p < 1.0
+        self.kernel = row_kernel_name(top_k, top_p, w.V)
+        self.out = L.alloc_outputs(w.n_target_rows, w.B, dev, want_conf=True)
+        self.ws = L.alloc_workspace(w.B, w.n_target_rows, dev)
+        self.kw = dict(max_len=spec.max_len, temperature=spec.temperature, top_k=top_k,
+                       top_p=top_p, mode=mode, out=self.out, workspace=self.ws, stream=stream)
+        self.calls = []
+        for st in self.sets:
+            a = (st.target, st.draft, st.draft_tokens, st.uniforms, st.verify_lens, st.row_offsets)
+            if self.filtered:
+                self.calls.append((L.prepare("spec_verify_rows", *a, **self.kw),
+                                   L.prepare("spec_verify_finalize", *a, **self.kw)))
+            else:
+                self.calls.append((L.prepare("spec_verify", *a, **self.kw), lambda: None))
+        self.launches = 2 if self.filtered else 1
+        self.positions = w.n_draft_rows
+        self.bytes = w.logit_bytes()
+        self.l2_cover = self.bytes * len(self.sets) > 2 * L2_BYTES
+
+
+def time_steps(prep, K, stream, flush=None, end=None):
+    """K steps; per step CUDA events around the row launch and around the
+    whole step (both on the launch stream).  ``flush``: a buffer larger than
+    L2 overwritten before each step, outside the events.  ``end``: an event
+    recorded after the last step, before the host waits.  Returns (per-step
+    row-launch ms, per-step ms)."""
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    for i in range(K):
+        if flush is not None:
+            flush.add_(1)
+        rows, fin = prep.calls[i % len(prep.calls)]
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        rows()
+        e1.record(stream)
+        fin()
+        e2.record(stream)
+    if end is not None:
+        end.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b, _ in ev], [a.elapsed_time(c) for a, _, c in ev]
+
+
+def measure_workload(L, spec, mode, dev, stream, top_k, top_p, oracle_budget_s, flush):
+    """One entry of ``per_workload``: drafted positions/s over the summed step
+    times, the dominant kernel's mean launch time and its fraction of the HBM
+    peak, and the oracle's check of one call on a sample of requests."""
+    prep = Prepared(L, spec, mode, dev, stream, seed=5000 + 7 * WORKLOAD_INDEX[spec.name],
+                    top_k=top_k, top_p=top_p)
+    use_flush = None if prep.l2_cover else flush
+    rows_ms, step_ms = time_steps(prep, 5, stream, use_flush)  # warm-up and size
+    assert int(prep.out.dev_error.item()) == 0, f"device error flags on {spec.name}"
+    K = int(max(20, min(2000, 0.5e3 / max(1e-3, statistics.fmean(step_ms)))))
+    rows_ms, step_ms = time_steps(prep, K, stream, use_flush)
+    assert int(prep.out.dev_error.item()) == 0, f"device error flags on {spec.name}"
+    peak, _ = hbm_peak()
+    kernel_ms = statistics.fmean(rows_ms)
+    gbs = prep.bytes / (kernel_ms / 1e3) / 1e9
+    ent = {"workload": spec.name, "mode": "sample" if mode == W.SAMPLE else "greedy",
+           "B": prep.w.B, "V": prep.w.V, "logits": spec.dtype, "top_k": top_k, "top_p": top_p,
+           "positions_per_s": prep.positions * K / (sum(step_ms) / 1e3),
+           "ms_per_step": statistics.fmean(step_ms), "steps": K,
+           "launches_per_step": prep.launches, "kernel": prep.kernel,
+           "kernel_mean_ms": kernel_ms, "bytes_per_launch": prep.bytes,
+           "achieved_gbs": gbs, "frac": gbs / peak,
+           "traffic": recorded_traffic(prep.kernel, spec.name),
+           "l2": ("inputs larger than L2: input sets alternate" if prep.l2_cover
+                  else "L2 flushed before each step (outside the events)")}
+    if oracle_budget_s > 0:
+        # one more call, then the oracle on a sample of its requests
+        prep.out.dev_error.zero_()
+        rows, fin = prep.calls[0]
+        rows()
+        fin()
+        torch.cuda.synchronize()
+        counts, rate, secs = oracle_check(prep.w, prep.out, spec, mode, top_k, top_p,
+                                          oracle_budget_s)
+        ent["oracle_check"] = counts
+        ent["oracle_positions_per_s"] = rate
+        ent["oracle_seconds"] = secs
+    del prep
+    torch.cuda.empty_cache()
+    return ent
+
+
+WORKLOAD_INDEX = {s.name: i for i, s in enumerate(W.WORKLOADS)}
+
+
 def run_ours(args, world, rank, local):
     from speculative_decoding_verification_16_gb300 import binding as L
 
@@ -271,95 +450,79 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(dev)
     spec = W.WORKLOADS[args.workload]
     mode = W.SAMPLE if args.mode == "sample" else W.GREEDY
-    seed = 1000 * args.workload + rank
-    kw = {"B": args.requests} if args.requests > 0 else {}
-    sets = [W.make_workload(spec, mode, seed=seed + 100 * i, device=dev, **kw) for i in range(2)]
-    w = sets[0]
-    B, Nt, Nd, V = w.B, w.n_target_rows, w.n_draft_rows, w.V
     stream = torch.cuda.current_stream(dev)
-    out = L.alloc_outputs(Nt, B, dev, want_conf=True)
-    ws = L.alloc_workspace(B, Nt, dev)
     top_k = spec.top_k if args.top_k is None else args.top_k
     top_p = spec.top_p if args.top_p is None else args.top_p
-    kw = dict(max_len=spec.max_len, temperature=spec.temperature, top_k=top_k,
-              top_p=top_p, mode=mode, out=out, workspace=ws, stream=stream)
-    # unfiltered: one launch per step (the rows kernel finishes the requests
-    # in its tail), timed whole; filtered: the row kernel, timed alone, then
-    # the request kernel
-    filtered = (0 < top_k < V) or top_p < 1.0
-    # kept sets of at most 64 tokens take the small-set row kernel
-    row_kernel = ("filter_rows_kernel" if 0 < top_k <= 64 else "gfilter_rows_kernel") \
-        if filtered else "rows_kernel"
-    calls = []
-    for s in sets:
-        args_ = (s.target, s.draft, s.draft_tokens, s.uniforms, s.verify_lens, s.row_offsets)
-        if filtered:
-            calls.append((L.prepare("spec_verify_rows", *args_, **kw),
-                          L.prepare("spec_verify_finalize", *args_, **kw)))
-        else:
-            calls.append((L.prepare("spec_verify", *args_, **kw), lambda: None))
-    launches_per_step = 2 if filtered else 1
-    # (sets use their own lengths; for ragged workloads the second set is
-    # drawn with a different seed, so row counts may differ)
-    n_rows = [s.n_target_rows + s.n_draft_rows for s in sets]
-    n_pos = [s.n_draft_rows for s in sets]
-    if n_rows[0] != n_rows[1]:
-        sets, calls, n_rows, n_pos = sets[:1], calls[:1], n_rows[:1], n_pos[:1]
+    prep = Prepared(L, spec, mode, dev, stream, seed=1000 * args.workload + rank, top_k=top_k,
+                    top_p=top_p, requests=args.requests)
+    w, out = prep.w, prep.out
+    B, V = w.B, w.V
+    flush = None
+    if not prep.l2_cover:  # small workloads: overwrite 2 x L2 before each step
+        flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
     for i in range(args.warmup):
-        rows, fin = calls[i % len(calls)]
+        if flush is not None:
+            flush.add_(1)
+        rows, fin = prep.calls[i % len(prep.calls)]
         rows()
         fin()
     torch.cuda.synchronize(dev)
     assert int(out.dev_error.item()) == 0, "device error flags during warm-up"
 
     K = args.steps
-    ev_rows = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     time.sleep(0.3 if sampler else 0.0)
     barrier(world)
     torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    positions = 0
-    for i in range(K):
-        rows, fin = calls[i % len(calls)]
-        e0, e1 = ev_rows[i]
-        e0.record(stream)
-        rows()
-        e1.record(stream)
-        fin()
-        positions += n_pos[i % len(calls)]
-    end.record(stream)
-    torch.cuda.synchronize(dev)
+    rows_ms, step_ms = time_steps(prep, K, stream, flush, end=end)
     barrier(world)
     clocks = sampler.stop() if sampler else None
-    elapsed_ms = start.elapsed_time(end)
-    rows_ms = [a.elapsed_time(b) for a, b in ev_rows]
+    # with a flush, only the steps' own events count; else the whole loop
+    elapsed_ms = sum(step_ms) if flush is not None else start.elapsed_time(end)
     elapsed_ms = max_over_ranks(elapsed_ms, world, dev)
-    total_pos = sum_over_ranks(positions, world, dev)
+    total_pos = sum_over_ranks(prep.positions * K, world, dev)
     value = total_pos / (elapsed_ms / 1e3)
     assert int(out.dev_error.item()) == 0, "device error flags during the timed steps"
 
-    esize = w.target.element_size()
-    bytes_per_launch = (sum(n_rows) / len(n_rows)) * V * esize
     mean_rows_ms = statistics.fmean(rows_ms)
-    achieved = bytes_per_launch / (mean_rows_ms / 1e3) / 1e9
+    achieved = prep.bytes / (mean_rows_ms / 1e3) / 1e9
     peak, peak_src = hbm_peak()
-    # the recorded traffic is for the full-size workload only
-    traffic = recorded_traffic(spec.name) if args.requests <= 0 else None
+    traffic = recorded_traffic(prep.kernel, spec.name) if args.requests <= 0 else None
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(L, sets[0], spec, mode, dev, stream, kw, K, world)
+        e2e = run_e2e(L, w, spec, mode, dev, stream, prep.kw, K, world)
 
     cpu = None
+    host_cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        rate, pos, secs, nreq = oracle_rate(w, spec, mode, 10.0, top_k=top_k, top_p=top_p)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{nreq} whole requests ({pos} drafted positions) of the same "
-                         f"workload, {secs:.1f} s of single-thread fp64 oracle time"}
+        counts, rate, secs = oracle_check(w, out, spec, mode, top_k, top_p, 8.0)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "host_cores": host_cores,
+               "host_cpu_count": os.cpu_count(), "kind": "oracle",
+               "sample": f"{counts['requests']} whole requests ({counts['positions']} drafted "
+                         f"positions) of the same workload, {secs:.1f} s of single-thread fp64 "
+                         f"oracle time",
+               "oracle_check": counts}
+    l2_note = (f"inputs larger than L2: {len(prep.sets)} input sets of "
+               f"{prep.bytes / 1e6:.0f} MB alternate between steps" if flush is None
+               else "L2 flushed before each step (outside the step events)")
+    launches = prep.launches
+    per = None
+    if rank == 0 and world == 1 and not args.no_per_workload:
+        del prep
+        torch.cuda.empty_cache()
+        per = []
+        if flush is None:
+            flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+        budget = 0.0 if args.no_cpu_baseline else 3.0
+        for idx, sp in enumerate(W.WORKLOADS):
+            for m in sp.modes:
+                mm = W.SAMPLE if m == "sample" else W.GREEDY
+                per.append(measure_workload(L, sp, mm, dev, stream, sp.top_k, sp.top_p, budget,
+                                            flush))
 
     if rank == 0:
         line = {
@@ -370,17 +533,17 @@ def run_ours(args, world, rank, local):
                        "logits": spec.dtype, "mode": args.mode,
                        "temperature": spec.temperature, "top_k": top_k,
                        "top_p": top_p, "labels": True,
-                       "l2": f"inputs larger than L2: {len(sets)} input sets of "
-                             f"{bytes_per_launch / 1e6:.0f} MB alternate between steps",
+                       "l2": l2_note,
                        "parallelism": f"replicas x{world} (independent batches)"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": row_kernel,
-                         "bytes_per_launch": bytes_per_launch,
+                         "kernel": row_kernel_name(top_k, top_p, V),
+                         "bytes_per_launch": w.logit_bytes(),
                          "mean_launch_ms": mean_rows_ms, "peak_source": peak_src},
-            "hbm_gbs_step": bytes_per_launch / (elapsed_ms / K / 1e3) / 1e9,
+            "hbm_gbs_step": w.logit_bytes() / (elapsed_ms / K / 1e3) / 1e9,
             "e2e": e2e, "cpu_baseline": cpu, "clocks": clocks,
-            "gpu_launches": launches_per_step * K,
+            "gpu_launches": launches * K,
+            "per_workload": per,
         }
         print(json.dumps(line), flush=True)
 
