@@ -237,7 +237,6 @@ __device__ __forceinline__ bool finish_request(const Params& P, int32_t r, const
                                                bool wait_ready, uint32_t& phase) {
   constexpr int NT = NW * 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int* ired = reinterpret_cast<int*>(fs.red);
 
   // ---- inputs only (before the rows kernel has finished, when launched as
   //      its dependent)

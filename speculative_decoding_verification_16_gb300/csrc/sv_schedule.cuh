@@ -107,7 +107,7 @@ __device__ __forceinline__ void merge_level(const uint64_t* ks, const uint16_t* 
 }
 
 __global__ void __launch_bounds__(kScheduleThreads) schedule_kernel(const ScheduleArgs A) {
-  extern __shared__ __align__(16) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x;
   const int N = A.B * A.K, NP = A.npad;
   uint64_t* key0 = reinterpret_cast<uint64_t*>(smem);
