@@ -34,8 +34,8 @@
 namespace sv {
 
 constexpr int kMaxK = SV_MAX_FILTER_K;  // 64
-constexpr int kCandCap = 2 * kMaxK;     // per-warp candidate buffer
-constexpr int kFilterCtasPerSm = 6;
+constexpr int kCandCap = 288;           // per-warp candidate buffer (31 left over + 256 new)
+constexpr int kFilterCtasPerSm = 5;
 
 struct FiltRow {
   int32_t n;       // kept tokens (<= k)
@@ -112,12 +112,68 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const unsigned char* p) {
   return v;
 }
 
+// Descending bitonic sort of one key per lane across the warp.
+__device__ __forceinline__ uint64_t warp_sort32_desc(uint64_t v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const uint64_t o = __shfl_xor_sync(0xffffffffu, v, j);
+      const bool desc = (lane & k) == 0;  // every lane at k = 32
+      v = (((lane & j) == 0) == desc) ? max(v, o) : min(v, o);
+    }
+  return v;
+}
+
+// The 32 largest keys of two descending lists (one key per lane), descending:
+// the element-wise larger of one list and the other reversed is a bitonic
+// sequence holding them, sorted by a bitonic merge.
+__device__ __forceinline__ uint64_t warp_merge_top32(uint64_t a, uint64_t b) {
+  const int lane = threadIdx.x & 31;
+  uint64_t c = max(a, __shfl_sync(0xffffffffu, b, 31 - lane));
+#pragma unroll
+  for (int j = 16; j > 0; j >>= 1) {
+    const uint64_t o = __shfl_xor_sync(0xffffffffu, c, j);
+    c = (lane & j) == 0 ? max(c, o) : min(c, o);
+  }
+  return c;
+}
+
+// Keys of one queued 16-byte vector (vector index k of the row) that beat the
+// bar `thr`, for one lane (valid: the lane holds an entry); NaN and +inf
+// are flagged, not kept.  Returns how many of the VEC keys beat the bar.
+template <int ES>
+__device__ __forceinline__ int vector_keys(const uint4& raw, int32_t k, bool valid, const Slice& s,
+                                           uint64_t thr, uint64_t* key, bool& bad) {
+  constexpr int VEC = 16 / ES;
+  const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+  const int32_t i0 = k * VEC - s.hoff;
+  int c = 0;
+#pragma unroll
+  for (int l = 0; l < VEC; ++l) {
+    const float x = ES == 2 ? ((l & 1) ? bf16hi(wv[l >> 1]) : bf16lo(wv[l >> 1]))
+                            : __uint_as_float(wv[l]);
+    const int32_t id = i0 + l;
+    const bool in = valid && id >= 0 && id < s.len;
+    if (in && (x != x || x == INFINITY)) bad = true;
+    key[l] = in && !(x != x)
+                 ? (static_cast<uint64_t>(order_key(x)) << 32) | static_cast<uint32_t>(~id)
+                 : 0ull;
+    c += key[l] > thr;
+  }
+  return c;
+}
+
+constexpr int kQCap = 64;  // per-warp queue of vectors that passed the screen
+
 template <int ES>
 __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel(const Params P) {
   constexpr int VEC = 16 / ES;
-  constexpr int UNROLL = 1;  // a short loop body: the kernel is bound by instruction supply
   __shared__ uint64_t cand[kWarps][kCandCap];
   __shared__ uint64_t merged[kWarps * kMaxK];
+  __shared__ __align__(16) uint4 qraw[kWarps][kQCap];  // queued vectors
+  __shared__ int32_t qidx[kWarps][kQCap];                // their vector indices
   __shared__ __align__(16) uint64_t bar_sh[kWarps];  // each warp's k-th best key
   __shared__ int bad_any;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -128,6 +184,8 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
   // the k-th best key seen so far
   int cap = 64;
   while (cap < K + 32) cap <<= 1;
+  int kp = 32;  // the warps' best K, padded to a power of two, for the final merge
+  while (kp < K) kp <<= 1;
   FiltRow* recs = reinterpret_cast<FiltRow*>(P.filt);
   const int32_t nrows = P.Nt + P.Nd;
   grid_dep_launch_dependents();
@@ -148,14 +206,131 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
     uint64_t thr = 0;   // warp-uniform: only larger keys can still make the top k
     float thr_val = -INFINITY;  // the logit of that key (the screen's bar)
     bool bad = false;
+    int qn = 0;         // warp-uniform: vectors waiting in the warp's queue
+    // k <= 32: the warp's best 32 keys so far, one per lane, descending; new
+    // candidates wait in the buffer and merge in 32 at a time
+    uint64_t top = 0ull;
+    const bool reg_list = K <= 32;
+
+    // Insert the keys of the first n queued vectors (lane l takes entry l):
+    // one scan when they all fit, else slot by slot, pruning (keep the best
+    // K, raise the bar) whenever a slot would not fit.
+    auto drain = [&](int n) {
+      const bool valid = lane < n;
+      const uint4 raw = valid ? qraw[warp][lane] : make_uint4(0, 0, 0, 0);
+      const int32_t k = valid ? qidx[warp][lane] : 0;
+      uint64_t key[VEC];
+      const int c = vector_keys<ES>(raw, k, valid, s, thr, key, bad);
+      const int total = __reduce_add_sync(0xffffffffu, c);
+      if (total == 0) return;
+      if (reg_list) {
+        int pre = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, pre, o);
+          if (lane >= o) pre += y;
+        }
+        int at = cnt + pre - c;
+#pragma unroll
+        for (int l = 0; l < VEC; ++l)
+          if (key[l] > thr) my[at++] = key[l];
+        cnt += total;
+        __syncwarp();
+        int base = 0;
+        for (; cnt - base >= 32; base += 32)
+          top = warp_merge_top32(top, warp_sort32_desc(my[base + lane]));
+        if (base > 0) {
+          // the bar: the k-th best key so far (it is in the list itself)
+          const uint64_t kth = __shfl_sync(0xffffffffu, top, K - 1);
+          if (kth > thr) {
+            thr = kth;
+            thr_val = key_value(thr);
+            if (lane == 0) bar_sh[warp] = thr;
+          }
+          const int rest = cnt - base;  // the rest (< 32) to the front
+          const uint64_t r = lane < rest ? my[base + lane] : 0ull;
+          __syncwarp();
+          if (lane < rest) my[lane] = r;
+          __syncwarp();
+          cnt = rest;
+        }
+        return;
+      }
+      if (cnt + total <= cap) {
+        int pre = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, pre, o);
+          if (lane >= o) pre += y;
+        }
+        int at = cnt + pre - c;
+#pragma unroll
+        for (int l = 0; l < VEC; ++l)
+          if (key[l] > thr) my[at++] = key[l];
+        cnt += total;
+        return;
+      }
+#pragma unroll
+      for (int l = 0; l < VEC; ++l) {
+        bool take = key[l] > thr;
+        unsigned m = __ballot_sync(0xffffffffu, take);
+        if (!m) continue;
+        if (cnt + __popc(m) > cap) {
+          cnt = warp_prune(my, cnt, K, cap);
+          if (cnt >= K && my[K - 1] > thr) {
+            thr = my[K - 1];
+            thr_val = key_value(thr);
+            if (lane == 0) bar_sh[warp] = thr;
+          }
+          take = key[l] > thr;
+          m = __ballot_sync(0xffffffffu, take);
+        }
+        if (take) my[cnt + __popc(m & lt_mask)] = key[l];
+        cnt += __popc(m);
+      }
+    };
+
     // the loop runs on the warp's first vector, so that every lane takes
-    // part in the warp-wide votes below; lanes past the end hold no element
-    int iter = 0;
-    for (int32_t kw = warp * 32; kw < nv; kw += UNROLL * kThreads, ++iter) {
+    // part in the warp-wide votes below; lanes past the end hold no element;
+    // each step loads the next step's vector before screening its own
+    int32_t kw = warp * 32;
+    uint4 nxt = kw + lane < nv ? ldg_nc_v4(s.gsrc + 16 * static_cast<size_t>(kw + lane))
+                               : make_uint4(0, 0, 0, 0);
+    // a first bar before any prune (k <= 32): just below the k-th largest of
+    // the lanes' first-vector maximum keys.  At least k keys of the row are
+    // above it (those maxima), so no key at or below it can be among the
+    // best k.
+    if (K <= 32) {
+      uint64_t key[VEC];
+      bool seed_bad = false;
+      vector_keys<ES>(nxt, kw + lane, kw + lane < nv, s, 0ull, key, seed_bad);
+      uint64_t mk = key[0];
+#pragma unroll
+      for (int l = 1; l < VEC; ++l) mk = max(mk, key[l]);
+      int above = 0;  // lanes whose maximum key is larger than this lane's
+#pragma unroll 8
+      for (int o = 0; o < 32; ++o) above += __shfl_sync(0xffffffffu, mk, o) > mk;
+      // the lane of rank k - 1 holds the k-th largest (keys are unique; lanes
+      // past the row hold 0, which never seeds)
+      const unsigned r = __ballot_sync(0xffffffffu, above == K - 1 && mk != 0ull);
+      if (r) {
+        // one below that key, so that the maximum itself still enters the
+        // buffer (the low half, a complemented id, is never zero: the value
+        // half is unchanged)
+        thr = __shfl_sync(0xffffffffu, mk, __ffs(r) - 1) - 1ull;
+        thr_val = key_value(thr);
+        if (lane == 0) bar_sh[warp] = thr;
+      }
+    }
+    for (; kw < nv; kw += kThreads) {
+      const int32_t k = kw + lane;
+      const uint4 raw = nxt;
+      if (kw + kThreads < nv)
+        nxt = k + kThreads < nv ? ldg_nc_v4(s.gsrc + 16 * static_cast<size_t>(k + kThreads))
+                                : make_uint4(0, 0, 0, 0);
       // any warp's k-th best key bars the whole CTA: an element below it
       // cannot be among the CTA's k best, so the highest of them is used
-      // (read every fourth step: a stale bar only lets more vectors through)
-      if ((iter & 3) == 0) {
+      {
         uint64_t b = thr;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) b = max(b, bar_sh[w]);
@@ -164,108 +339,85 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
           thr_val = key_value(b);
         }
       }
-      uint4 raw[UNROLL];
-#pragma unroll
-      for (int q = 0; q < UNROLL; ++q) {
-        const int32_t k = kw + lane + q * kThreads;
-        raw[q] = k < nv ? ldg_nc_v4(s.gsrc + 16 * static_cast<size_t>(k)) : make_uint4(0, 0, 0, 0);
+      // screen: a vector whose largest logit is below the bar holds no
+      // candidate (a NaN maximum is queued and flagged); bf16 vectors take
+      // their maximum on the packed pairs
+      float vm;
+      if (ES == 2) {
+        const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(raw.x, raw.y), bf16x2_max_nan(raw.z, raw.w));
+        vm = fmax_nan(bf16lo(m2), bf16hi(m2));
+      } else {
+        vm = fmax_nan(fmax_nan(__uint_as_float(raw.x), __uint_as_float(raw.y)),
+                      fmax_nan(__uint_as_float(raw.z), __uint_as_float(raw.w)));
       }
-#pragma unroll
-      for (int q = 0; q < UNROLL; ++q) {
-        const int32_t k = kw + lane + q * kThreads;
-        if (kw + q * kThreads >= nv) break;  // warp-uniform
-        const uint32_t wv[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
-        // screen: a vector whose largest logit is below the warp's bar holds
-        // no candidate (a NaN maximum goes on to the exact path and is
-        // flagged); bf16 vectors take their maximum on the packed pairs
-        float vm;
-        if (ES == 2) {
-          const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(wv[0], wv[1]),
-                                             bf16x2_max_nan(wv[2], wv[3]));
-          vm = fmax_nan(bf16lo(m2), bf16hi(m2));
-        } else {
-          vm = fmax_nan(fmax_nan(__uint_as_float(wv[0]), __uint_as_float(wv[1])),
-                        fmax_nan(__uint_as_float(wv[2]), __uint_as_float(wv[3])));
+      const bool maybe = k < nv && !(vm < thr_val);
+      const unsigned mq = __ballot_sync(0xffffffffu, maybe);
+      if (mq == 0) continue;
+      // queue the vectors that passed; keys are formed once 32 are waiting
+      if (maybe) {
+        const int at = qn + __popc(mq & lt_mask);
+        qraw[warp][at] = raw;
+        qidx[warp][at] = k;
+      }
+      qn += __popc(mq);
+      __syncwarp();
+      if (qn >= 32) {
+        drain(32);
+        // move the rest (at most 31) to the front
+        const int rest = qn - 32;
+        uint4 r4;
+        int32_t ri = 0;
+        if (lane < rest) {
+          r4 = qraw[warp][32 + lane];
+          ri = qidx[warp][32 + lane];
         }
-        const bool maybe = k < nv && !(vm < thr_val);
-        if (!__any_sync(0xffffffffu, maybe)) continue;
-        float x[VEC];
-#pragma unroll
-        for (int l = 0; l < VEC; ++l)
-          x[l] = ES == 2 ? ((l & 1) ? bf16hi(wv[l >> 1]) : bf16lo(wv[l >> 1]))
-                         : __uint_as_float(wv[l]);
-        const int32_t i0 = k * VEC - s.hoff;
-        // this lane's keys above the bar (NaN and +inf are flagged, not kept)
-        uint64_t key[VEC];
-        int c = 0;
-#pragma unroll
-        for (int l = 0; l < VEC; ++l) {
-          const int32_t id = i0 + l;
-          const bool valid = maybe && id >= 0 && id < s.len;
-          if (valid && (x[l] != x[l] || x[l] == INFINITY)) bad = true;
-          key[l] = valid && !(x[l] != x[l])
-                       ? (static_cast<uint64_t>(order_key(x[l])) << 32) | static_cast<uint32_t>(~id)
-                       : 0ull;
-          c += key[l] > thr;
+        __syncwarp();
+        if (lane < rest) {
+          qraw[warp][lane] = r4;
+          qidx[warp][lane] = ri;
         }
-        int total = __reduce_add_sync(0xffffffffu, c);
-        if (total == 0) continue;
-        if (cnt + total <= cap) {  // one scan places every lane's keys
-          int pre = c;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, pre, o);
-            if (lane >= o) pre += y;
-          }
-          int at = cnt + pre - c;
-#pragma unroll
-          for (int l = 0; l < VEC; ++l)
-            if (key[l] > thr) my[at++] = key[l];
-          cnt += total;
-          continue;
-        }
-        // the buffer could overflow: element slot by element slot, pruning
-        // (keep the best K, raise the bar) whenever a slot would not fit
-#pragma unroll
-        for (int l = 0; l < VEC; ++l) {
-          bool take = key[l] > thr;
-          unsigned m = __ballot_sync(0xffffffffu, take);
-          if (!m) continue;
-          if (cnt + __popc(m) > cap) {
-            cnt = warp_prune(my, cnt, K, cap);
-            if (cnt >= K && my[K - 1] > thr) {
-              thr = my[K - 1];
-              thr_val = key_value(thr);
-              if (lane == 0) bar_sh[warp] = thr;
-            }
-            take = key[l] > thr;
-            m = __ballot_sync(0xffffffffu, take);
-          }
-          if (take) my[cnt + __popc(m & lt_mask)] = key[l];
-          cnt += __popc(m);
-        }
+        __syncwarp();
+        qn = rest;
       }
     }
-    cnt = warp_prune(my, cnt, K, cap);
-    for (int i = lane; i < kMaxK; i += 32) merged[warp * kMaxK + i] = i < K ? my[i] : 0ull;
+    if (qn > 0) drain(qn);
+    if (reg_list) {
+      top = warp_merge_top32(top, warp_sort32_desc(lane < cnt ? my[lane] : 0ull));
+      merged[warp * kp + lane] = lane < K ? top : 0ull;  // kp = 32
+    } else {
+      cnt = warp_prune(my, cnt, K, cap);
+      for (int i = lane; i < kp; i += 32) merged[warp * kp + i] = i < K ? my[i] : 0ull;
+    }
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&bad_any, 1);
     __syncthreads();
-    // the CTA's best K of the warps' best K: bitonic sort of kWarps * kMaxK keys
-    constexpr int NM = kWarps * kMaxK;
-    for (int kk = 2; kk <= NM; kk <<= 1) {
-      for (int j = kk >> 1; j > 0; j >>= 1) {
-        for (int i = tid; i < NM; i += kThreads) {
-          const int p = i ^ j;
-          if (p > i) {
-            const uint64_t a = merged[i], b = merged[p];
-            const bool desc = (i & kk) == 0;
-            if (desc ? (a < b) : (a > b)) {
-              merged[i] = b;
-              merged[p] = a;
+    if (reg_list) {
+      // the CTA's best 32: warp 0 folds the warps' sorted lists together
+      if (warp == 0) {
+        uint64_t t = merged[lane];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) t = warp_merge_top32(t, merged[w * 32 + lane]);
+        merged[lane] = t;
+        merged[32 + lane] = 0ull;
+        __syncwarp();
+      }
+    } else {
+    // the CTA's best K of the warps' best K: bitonic sort of kWarps * kp keys
+      const int NM = kWarps * kp;
+      for (int kk = 2; kk <= NM; kk <<= 1) {
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+          for (int i = tid; i < NM; i += kThreads) {
+            const int p = i ^ j;
+            if (p > i) {
+              const uint64_t a = merged[i], b = merged[p];
+              const bool desc = (i & kk) == 0;
+              if (desc ? (a < b) : (a > b)) {
+                merged[i] = b;
+                merged[p] = a;
+              }
             }
           }
+          __syncthreads();
         }
-        __syncthreads();
       }
     }
     if (warp == 0) {
