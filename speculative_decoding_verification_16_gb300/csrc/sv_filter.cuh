@@ -322,6 +322,7 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
         if (lane == 0) bar_sh[warp] = thr;
       }
     }
+    int step = 0;
     for (; kw < nv; kw += kThreads) {
       const int32_t k = kw + lane;
       const uint4 raw = nxt;
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
                                 : make_uint4(0, 0, 0, 0);
       // any warp's k-th best key bars the whole CTA: an element below it
       // cannot be among the CTA's k best, so the highest of them is used
-      {
+      // (read every eighth step: a stale bar only lets more vectors through)
+      if ((++step & 7) == 0) {
         uint64_t b = thr;
 #pragma unroll
         for (int w = 0; w < kWarps; ++w) b = max(b, bar_sh[w]);
