@@ -361,8 +361,14 @@ int run_rows(const Args& a, bool fuse) {
   if (P.top_k > 0) {  // top-k / top-p: one streaming pass per row, no exchange
     const int rows = P.Nt + P.Nd;
     const int grid = std::max(1, std::min(rows, dc.sms * kFilterCtasPerSm));
-    if (es == 2) filter_rows_kernel<2><<<grid, kThreads, 0, st>>>(P);
-    else filter_rows_kernel<4><<<grid, kThreads, 0, st>>>(P);
+    const bool two = P.top_k > 32;  // kept lists of 64 keys per warp
+    if (es == 2) {
+      if (two) filter_rows_kernel<2, true><<<grid, kThreads, 0, st>>>(P);
+      else filter_rows_kernel<2, false><<<grid, kThreads, 0, st>>>(P);
+    } else {
+      if (two) filter_rows_kernel<4, true><<<grid, kThreads, 0, st>>>(P);
+      else filter_rows_kernel<4, false><<<grid, kThreads, 0, st>>>(P);
+    }
     return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
   }
   RowsGeom geo;

@@ -35,7 +35,11 @@ namespace sv {
 
 constexpr int kMaxK = SV_MAX_FILTER_K;  // 64
 constexpr int kCandCap = 288;           // per-warp candidate buffer (31 left over + 256 new)
-constexpr int kFilterCtasPerSm = 5;
+// 16-byte loads each thread keeps in flight while it screens (the row is
+// streamed with plain loads, so this sets the bytes in flight per SM), and
+// the CTAs per SM that the registers then allow
+constexpr int kFilterDepth = 2;
+constexpr int kFilterCtasPerSm = kFilterDepth > 1 ? 4 : 5;
 
 struct FiltRow {
   int32_t n;       // kept tokens (<= k)
@@ -67,42 +71,6 @@ __device__ __forceinline__ int32_t key_id(uint64_t c) {
   return static_cast<int32_t>(~static_cast<uint32_t>(c));
 }
 
-// Sort n (a power of two, <= 2 * 32 * per) keys of a warp's shared buffer in
-// descending order (bitonic network; entries >= count must already be 0).
-__device__ __forceinline__ void warp_sort_desc(uint64_t* a, int n) {
-  const int lane = threadIdx.x & 31;
-  for (int k = 2; k <= n; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      __syncwarp();
-      for (int i = lane; i < n; i += 32) {
-        const int p = i ^ j;
-        if (p > i) {
-          const uint64_t x = a[i], y = a[p];
-          const bool desc = (i & k) == 0;
-          if (desc ? (x < y) : (x > y)) {
-            a[i] = y;
-            a[p] = x;
-          }
-        }
-      }
-    }
-  }
-  __syncwarp();
-}
-
-// Keep the kmax largest of the first `cap` keys of a warp's buffer (sorted,
-// descending) and return the new count; entries beyond it are cleared.
-__device__ __forceinline__ int warp_prune(uint64_t* cand, int cnt, int kmax, int cap) {
-  const int lane = threadIdx.x & 31;
-  __syncwarp();
-  for (int i = cnt + lane; i < cap; i += 32) cand[i] = 0;
-  warp_sort_desc(cand, cap);
-  const int keep = min(cnt, kmax);
-  for (int i = keep + lane; i < cap; i += 32) cand[i] = 0;
-  __syncwarp();
-  return keep;
-}
-
 // 16-byte read-only load that does not allocate in L1.
 __device__ __forceinline__ uint4 ldg_nc_v4(const unsigned char* p) {
   uint4 v;
@@ -126,18 +94,68 @@ __device__ __forceinline__ uint64_t warp_sort32_desc(uint64_t v) {
   return v;
 }
 
-// The 32 largest keys of two descending lists (one key per lane), descending:
-// the element-wise larger of one list and the other reversed is a bitonic
-// sequence holding them, sorted by a bitonic merge.
-__device__ __forceinline__ uint64_t warp_merge_top32(uint64_t a, uint64_t b) {
+// Sort a bitonic sequence of keys (one per lane) into descending order.
+__device__ __forceinline__ uint64_t warp_bitonic_desc(uint64_t c) {
   const int lane = threadIdx.x & 31;
-  uint64_t c = max(a, __shfl_sync(0xffffffffu, b, 31 - lane));
 #pragma unroll
   for (int j = 16; j > 0; j >>= 1) {
     const uint64_t o = __shfl_xor_sync(0xffffffffu, c, j);
     c = (lane & j) == 0 ? max(c, o) : min(c, o);
   }
   return c;
+}
+
+// The 32 largest keys of two descending lists (one key per lane), descending:
+// the element-wise larger of one list and the other reversed is a bitonic
+// sequence holding them.
+__device__ __forceinline__ uint64_t warp_merge_top32(uint64_t a, uint64_t b) {
+  return warp_bitonic_desc(max(a, __shfl_sync(0xffffffffu, b, 31 - (threadIdx.x & 31))));
+}
+
+// A warp's best keys so far, descending: ranks 0..31 in hi (lane i holds
+// rank i) and, when more than 32 are kept (TWO), ranks 32..63 in lo.
+// Empty ranks hold 0, which is below every key.
+struct TopList {
+  uint64_t hi, lo;
+};
+
+// Merge 32 keys (one per lane, descending) into the list.
+template <bool TWO>
+__device__ __forceinline__ void list_insert(TopList& t, uint64_t c) {
+  const uint64_t cr = __shfl_sync(0xffffffffu, c, 31 - (threadIdx.x & 31));
+  if (!TWO) {
+    t.hi = warp_bitonic_desc(max(t.hi, cr));
+    return;
+  }
+  // every lo key is below every hi key, so the best 32 of hi and c are the
+  // best 32 overall; the other 32 of them compete with lo for ranks 32..63
+  const uint64_t up = max(t.hi, cr), down = min(t.hi, cr);
+  t.hi = warp_bitonic_desc(up);
+  t.lo = warp_merge_top32(t.lo, warp_bitonic_desc(down));
+}
+
+// a := the best 32 (64 with TWO) keys of the lists a and b.
+template <bool TWO>
+__device__ __forceinline__ void list_merge(TopList& a, const TopList& b) {
+  if (!TWO) {
+    a.hi = warp_merge_top32(a.hi, b.hi);
+    return;
+  }
+  // element i of a against element 63 - i of b: the larger ones form a
+  // bitonic sequence of 64 holding the best 64; its first merge stage pairs
+  // rank i with rank i + 32, then each half is bitonic
+  const int rev = 31 - (threadIdx.x & 31);
+  const uint64_t ch = max(a.hi, __shfl_sync(0xffffffffu, b.lo, rev));
+  const uint64_t cl = max(a.lo, __shfl_sync(0xffffffffu, b.hi, rev));
+  a.hi = warp_bitonic_desc(max(ch, cl));
+  a.lo = warp_bitonic_desc(min(ch, cl));
+}
+
+// The key of rank j (0-based, warp-uniform, j < 32 or, with TWO, j < 64).
+template <bool TWO>
+__device__ __forceinline__ uint64_t list_rank(const TopList& t, int j) {
+  if (TWO && j >= 32) return __shfl_sync(0xffffffffu, t.lo, j - 32);
+  return __shfl_sync(0xffffffffu, t.hi, j & 31);
 }
 
 // Keys of one queued 16-byte vector (vector index k of the row) that beat the
@@ -165,27 +183,70 @@ __device__ __forceinline__ int vector_keys(const uint4& raw, int32_t k, bool val
   return c;
 }
 
-constexpr int kQCap = 64;  // per-warp queue of vectors that passed the screen
-
+// Largest logit of one 16-byte vector, NaN if any element is NaN (bf16
+// vectors take the maximum on the packed pairs first).
 template <int ES>
+__device__ __forceinline__ float vec_max(const uint4& v) {
+  if (ES == 2) {
+    const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(v.x, v.y), bf16x2_max_nan(v.z, v.w));
+    return fmax_nan(bf16lo(m2), bf16hi(m2));
+  }
+  return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                  fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+}
+
+// Largest logit of N vectors, NaN if any element is NaN.
+template <int ES, int N>
+__device__ __forceinline__ float vecs_max(const uint4 (&v)[N]) {
+  if (ES == 2) {
+    uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(v[0].x, v[0].y), bf16x2_max_nan(v[0].z, v[0].w));
+#pragma unroll
+    for (int i = 1; i < N; ++i)
+      m2 = bf16x2_max_nan(m2, bf16x2_max_nan(bf16x2_max_nan(v[i].x, v[i].y),
+                                             bf16x2_max_nan(v[i].z, v[i].w)));
+    return fmax_nan(bf16lo(m2), bf16hi(m2));
+  }
+  float m = vec_max<ES>(v[0]);
+#pragma unroll
+  for (int i = 1; i < N; ++i) m = fmax_nan(m, vec_max<ES>(v[i]));
+  return m;
+}
+
+// per-warp queue of vectors that passed the screen: fewer than 32 waiting,
+// plus one iteration's worth
+constexpr int kQCap = 32 + 32 * kFilterDepth;
+
+// filter_rows_kernel: the k best keys of a row, k <= 32 (TWO false) or
+// k <= 64 (TWO true).
+//
+// Each warp streams its vectors (vector warp * 32 + lane, then kThreads on)
+// and screens them against a bar: a key at or below it cannot be among the
+// row's k best.  Vectors that pass wait in a per-warp queue; 32 of them at a
+// time become keys, those above the bar are staged, and staged keys merge 32
+// at a time into the warp's register list of its best keys.  Every bar
+// below is valid because it has at least k keys of the row above it:
+//  - a warp's own k-th best key;
+//  - the m-th largest of the warps' published rank-r keys (r = ceil(k / 8),
+//    m = ceil(k / r)): m warps each hold r keys at or above it, m r >= k
+//    keys in all, and the warps' keys are distinct elements of the row;
+//  - before any list fills (k <= 32), the k-th largest of the maxima of the
+//    warp's first 32 vectors (k distinct elements at or above it).
+// A bar that one warp finds serves the whole CTA through a shared word.
+template <int ES, bool TWO>
 __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel(const Params P) {
   constexpr int VEC = 16 / ES;
-  __shared__ uint64_t cand[kWarps][kCandCap];
-  __shared__ uint64_t merged[kWarps * kMaxK];
+  __shared__ uint64_t cand[kWarps][kCandCap];  // staged keys, per warp
+  __shared__ uint64_t lists[kWarps][64];        // the warps' lists, at the end of a row
   __shared__ __align__(16) uint4 qraw[kWarps][kQCap];  // queued vectors
   __shared__ int32_t qidx[kWarps][kQCap];                // their vector indices
-  __shared__ __align__(16) uint64_t bar_sh[kWarps];  // each warp's k-th best key
+  __shared__ uint64_t pub[kWarps];  // each warp's key of rank r - 1 (0: fewer than r)
+  __shared__ uint64_t cta_bar;      // the best bar any warp has found
   __shared__ int bad_any;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
   const int K = P.top_k;
-  // buffer in use: the smallest power of two that holds k keys plus one
-  // vote's worth (32), so that the bar is raised often and stays close to
-  // the k-th best key seen so far
-  int cap = 64;
-  while (cap < K + 32) cap <<= 1;
-  int kp = 32;  // the warps' best K, padded to a power of two, for the final merge
-  while (kp < K) kp <<= 1;
+  const int r = (K + kWarps - 1) / kWarps;  // 1..8
+  const int m = (K + r - 1) / r;            // <= kWarps
   FiltRow* recs = reinterpret_cast<FiltRow*>(P.filt);
   const int32_t nrows = P.Nt + P.Nd;
   grid_dep_launch_dependents();
@@ -198,23 +259,50 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
     const Slice s = make_slice<ES>(base, P.V, 0, P.V);  // the whole row
     const int32_t nv = s.nbytes >> 4;
     uint64_t* my = cand[warp];
-    for (int i = lane; i < kCandCap; i += 32) my[i] = 0;
-    if (tid == 0) bad_any = 0;
-    if (tid < kWarps) bar_sh[tid] = 0ull;
+    if (tid == 0) {
+      bad_any = 0;
+      cta_bar = 0ull;
+    }
+    if (tid < kWarps) pub[tid] = 0ull;
     __syncthreads();
-    int cnt = 0;        // warp-uniform
-    uint64_t thr = 0;   // warp-uniform: only larger keys can still make the top k
+    int cnt = 0;                // warp-uniform: staged keys
+    uint64_t thr = 0;           // warp-uniform: the bar
     float thr_val = -INFINITY;  // the logit of that key (the screen's bar)
     bool bad = false;
-    int qn = 0;         // warp-uniform: vectors waiting in the warp's queue
-    // k <= 32: the warp's best 32 keys so far, one per lane, descending; new
-    // candidates wait in the buffer and merge in 32 at a time
-    uint64_t top = 0ull;
-    const bool reg_list = K <= 32;
+    int qn = 0;                 // warp-uniform: vectors waiting in the warp's queue
+    TopList top{0ull, 0ull};
 
-    // Insert the keys of the first n queued vectors (lane l takes entry l):
-    // one scan when they all fit, else slot by slot, pruning (keep the best
-    // K, raise the bar) whenever a slot would not fit.
+    // adopt a bar (warp-uniform) and share it
+    auto raise_to = [&](uint64_t nb) {
+      if (nb > thr) {
+        thr = nb;
+        thr_val = key_value(nb);
+        if (lane == 0) atomicMax(reinterpret_cast<unsigned long long*>(&cta_bar), nb);
+      }
+    };
+    // after the list changed: the warp's k-th best key, and the m-th largest
+    // of the published rank-r keys (this warp's own just updated)
+    auto list_bars = [&]() {
+      const uint64_t own = list_rank<TWO>(top, K - 1);
+      const uint64_t mine = list_rank<TWO>(top, r - 1);
+      if (lane == 0) pub[warp] = mine;
+      __syncwarp();
+      const uint64_t v = lane < kWarps ? *reinterpret_cast<volatile uint64_t*>(&pub[lane]) : 0ull;
+      int gt = 0, ge = 0;
+#pragma unroll
+      for (int j = 0; j < kWarps; ++j) {
+        const uint64_t o = __shfl_sync(0xffffffffu, v, j);
+        gt += o > v;
+        ge += o >= v;
+      }
+      const unsigned sel = __ballot_sync(0xffffffffu, lane < kWarps && gt < m && m <= ge);
+      const uint64_t q = sel ? __shfl_sync(0xffffffffu, v, __ffs(sel) - 1) : 0ull;
+      const uint64_t qb = q > 0ull ? q - 1ull : 0ull;
+      raise_to(own > qb ? own : qb);
+    };
+
+    // Keys of the first n queued vectors (lane l takes entry l) that beat
+    // the bar go to the staging buffer; full groups of 32 merge into the list.
     auto drain = [&](int n) {
       const bool valid = lane < n;
       const uint4 raw = valid ? qraw[warp][lane] : make_uint4(0, 0, 0, 0);
@@ -223,211 +311,137 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
       const int c = vector_keys<ES>(raw, k, valid, s, thr, key, bad);
       const int total = __reduce_add_sync(0xffffffffu, c);
       if (total == 0) return;
-      if (reg_list) {
-        int pre = c;
+      int pre = c;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, pre, o);
-          if (lane >= o) pre += y;
-        }
-        int at = cnt + pre - c;
-#pragma unroll
-        for (int l = 0; l < VEC; ++l)
-          if (key[l] > thr) my[at++] = key[l];
-        cnt += total;
-        __syncwarp();
-        int base = 0;
-        for (; cnt - base >= 32; base += 32)
-          top = warp_merge_top32(top, warp_sort32_desc(my[base + lane]));
-        if (base > 0) {
-          // the bar: the k-th best key so far (it is in the list itself)
-          const uint64_t kth = __shfl_sync(0xffffffffu, top, K - 1);
-          if (kth > thr) {
-            thr = kth;
-            thr_val = key_value(thr);
-            if (lane == 0) bar_sh[warp] = thr;
-          }
-          const int rest = cnt - base;  // the rest (< 32) to the front
-          const uint64_t r = lane < rest ? my[base + lane] : 0ull;
-          __syncwarp();
-          if (lane < rest) my[lane] = r;
-          __syncwarp();
-          cnt = rest;
-        }
-        return;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, pre, o);
+        if (lane >= o) pre += y;
       }
-      if (cnt + total <= cap) {
-        int pre = c;
+      int at = cnt + pre - c;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, pre, o);
-          if (lane >= o) pre += y;
-        }
-        int at = cnt + pre - c;
-#pragma unroll
-        for (int l = 0; l < VEC; ++l)
-          if (key[l] > thr) my[at++] = key[l];
-        cnt += total;
-        return;
-      }
-#pragma unroll
-      for (int l = 0; l < VEC; ++l) {
-        bool take = key[l] > thr;
-        unsigned m = __ballot_sync(0xffffffffu, take);
-        if (!m) continue;
-        if (cnt + __popc(m) > cap) {
-          cnt = warp_prune(my, cnt, K, cap);
-          if (cnt >= K && my[K - 1] > thr) {
-            thr = my[K - 1];
-            thr_val = key_value(thr);
-            if (lane == 0) bar_sh[warp] = thr;
-          }
-          take = key[l] > thr;
-          m = __ballot_sync(0xffffffffu, take);
-        }
-        if (take) my[cnt + __popc(m & lt_mask)] = key[l];
-        cnt += __popc(m);
-      }
+      for (int l = 0; l < VEC; ++l)
+        if (key[l] > thr) my[at++] = key[l];
+      cnt += total;  // < 32 + 32 VEC <= kCandCap
+      __syncwarp();
+      if (cnt < 32) return;
+      int done = 0;
+      for (; cnt - done >= 32; done += 32) list_insert<TWO>(top, warp_sort32_desc(my[done + lane]));
+      const int rest = cnt - done;  // the rest (< 32) to the front
+      const uint64_t rk = lane < rest ? my[done + lane] : 0ull;
+      __syncwarp();
+      if (lane < rest) my[lane] = rk;
+      __syncwarp();
+      cnt = rest;
+      list_bars();
     };
 
-    // the loop runs on the warp's first vector, so that every lane takes
-    // part in the warp-wide votes below; lanes past the end hold no element;
-    // each step loads the next step's vector before screening its own
-    int32_t kw = warp * 32;
-    uint4 nxt = kw + lane < nv ? ldg_nc_v4(s.gsrc + 16 * static_cast<size_t>(kw + lane))
-                               : make_uint4(0, 0, 0, 0);
-    // a first bar before any prune (k <= 32): just below the k-th largest of
-    // the lanes' first-vector maximum keys.  At least k keys of the row are
-    // above it (those maxima), so no key at or below it can be among the
-    // best k.
-    if (K <= 32) {
+    // The warp's vectors are k0 + j kThreads, j = 0, 1, ... (step j).  Each
+    // iteration screens kFilterDepth steps while the loads of the next
+    // kFilterDepth are in flight (clamped into the row, so that no load needs
+    // a branch; a clamped copy is never queued as a row element).
+    const int32_t k0 = warp * 32 + lane;
+    const int32_t rem = nv - warp * 32;
+    const int32_t nsteps = rem > 0 ? (rem - 1) / kThreads + 1 : 0;
+    auto load_step = [&](int32_t j) {
+      const int32_t k = min(k0 + j * kThreads, nv - 1);
+      return ldg_nc_v4(s.gsrc + 16 * static_cast<size_t>(k));
+    };
+    uint4 nxt[kFilterDepth];
+#pragma unroll
+    for (int d = 0; d < kFilterDepth; ++d) nxt[d] = load_step(d);
+    if (!TWO) {
+      // the first bar: just below the k-th largest of the lanes' first-vector
+      // maximum keys (so that the maximum itself still passes; the low half
+      // of a key, a complemented id, is never zero)
       uint64_t key[VEC];
       bool seed_bad = false;
-      vector_keys<ES>(nxt, kw + lane, kw + lane < nv, s, 0ull, key, seed_bad);
+      vector_keys<ES>(nxt[0], k0, k0 < nv, s, 0ull, key, seed_bad);
       uint64_t mk = key[0];
 #pragma unroll
       for (int l = 1; l < VEC; ++l) mk = max(mk, key[l]);
       int above = 0;  // lanes whose maximum key is larger than this lane's
 #pragma unroll 8
       for (int o = 0; o < 32; ++o) above += __shfl_sync(0xffffffffu, mk, o) > mk;
-      // the lane of rank k - 1 holds the k-th largest (keys are unique; lanes
-      // past the row hold 0, which never seeds)
-      const unsigned r = __ballot_sync(0xffffffffu, above == K - 1 && mk != 0ull);
-      if (r) {
-        // one below that key, so that the maximum itself still enters the
-        // buffer (the low half, a complemented id, is never zero: the value
-        // half is unchanged)
-        thr = __shfl_sync(0xffffffffu, mk, __ffs(r) - 1) - 1ull;
-        thr_val = key_value(thr);
-        if (lane == 0) bar_sh[warp] = thr;
-      }
+      // keys are unique; lanes past the row hold 0, which never seeds
+      const unsigned rk = __ballot_sync(0xffffffffu, above == K - 1 && mk != 0ull);
+      if (rk) raise_to(__shfl_sync(0xffffffffu, mk, __ffs(rk) - 1) - 1ull);
     }
-    int step = 0;
-    for (; kw < nv; kw += kThreads) {
-      const int32_t k = kw + lane;
-      const uint4 raw = nxt;
-      if (kw + kThreads < nv)
-        nxt = k + kThreads < nv ? ldg_nc_v4(s.gsrc + 16 * static_cast<size_t>(k + kThreads))
-                                : make_uint4(0, 0, 0, 0);
-      // any warp's k-th best key bars the whole CTA: an element below it
-      // cannot be among the CTA's k best, so the highest of them is used
-      // (read every eighth step: a stale bar only lets more vectors through)
-      if ((++step & 7) == 0) {
-        uint64_t b = thr;
+    for (int32_t j = 0; j < nsteps; j += kFilterDepth) {
+      uint4 cur[kFilterDepth];
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) b = max(b, bar_sh[w]);
-        if (b > thr) {
-          thr = b;
-          thr_val = key_value(b);
+      for (int d = 0; d < kFilterDepth; ++d) {
+        cur[d] = nxt[d];
+        nxt[d] = load_step(j + kFilterDepth + d);
+      }
+      // the best bar any warp has found (a stale one only lets more through)
+      const uint64_t cb = *reinterpret_cast<volatile uint64_t*>(&cta_bar);
+      if (cb > thr) {
+        thr = cb;
+        thr_val = key_value(cb);
+      }
+      // screen: no logit of these vectors reaches the bar (clamped copies
+      // past the row only make the test pass more often)
+      if (__ballot_sync(0xffffffffu, !(vecs_max<ES, kFilterDepth>(cur) < thr_val)) == 0) continue;
+      // queue each vector whose largest logit is not below the bar (a NaN
+      // maximum is queued and flagged by the drain)
+#pragma unroll
+      for (int d = 0; d < kFilterDepth; ++d) {
+        const int32_t k = k0 + (j + d) * kThreads;
+        const bool maybe = k < nv && !(vec_max<ES>(cur[d]) < thr_val);
+        const unsigned mq = __ballot_sync(0xffffffffu, maybe);
+        if (maybe) {
+          const int at = qn + __popc(mq & lt_mask);
+          qraw[warp][at] = cur[d];
+          qidx[warp][at] = k;
         }
+        qn += __popc(mq);
       }
-      // screen: a vector whose largest logit is below the bar holds no
-      // candidate (a NaN maximum is queued and flagged); bf16 vectors take
-      // their maximum on the packed pairs
-      float vm;
-      if (ES == 2) {
-        const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(raw.x, raw.y), bf16x2_max_nan(raw.z, raw.w));
-        vm = fmax_nan(bf16lo(m2), bf16hi(m2));
-      } else {
-        vm = fmax_nan(fmax_nan(__uint_as_float(raw.x), __uint_as_float(raw.y)),
-                      fmax_nan(__uint_as_float(raw.z), __uint_as_float(raw.w)));
-      }
-      const bool maybe = k < nv && !(vm < thr_val);
-      const unsigned mq = __ballot_sync(0xffffffffu, maybe);
-      if (mq == 0) continue;
-      // queue the vectors that passed; keys are formed once 32 are waiting
-      if (maybe) {
-        const int at = qn + __popc(mq & lt_mask);
-        qraw[warp][at] = raw;
-        qidx[warp][at] = k;
-      }
-      qn += __popc(mq);
       __syncwarp();
-      if (qn >= 32) {
+      while (qn >= 32) {
         drain(32);
-        // move the rest (at most 31) to the front
+        // move the rest (fewer than 32 kFilterDepth) to the front
         const int rest = qn - 32;
-        uint4 r4;
-        int32_t ri = 0;
-        if (lane < rest) {
-          r4 = qraw[warp][32 + lane];
-          ri = qidx[warp][32 + lane];
+        uint4 r4[kFilterDepth];
+        int32_t ri[kFilterDepth];
+#pragma unroll
+        for (int t = 0; t < kFilterDepth; ++t) {
+          const int i = lane + 32 * t;
+          if (i < rest) {
+            r4[t] = qraw[warp][32 + i];
+            ri[t] = qidx[warp][32 + i];
+          }
         }
         __syncwarp();
-        if (lane < rest) {
-          qraw[warp][lane] = r4;
-          qidx[warp][lane] = ri;
+#pragma unroll
+        for (int t = 0; t < kFilterDepth; ++t) {
+          const int i = lane + 32 * t;
+          if (i < rest) {
+            qraw[warp][i] = r4[t];
+            qidx[warp][i] = ri[t];
+          }
         }
         __syncwarp();
         qn = rest;
       }
     }
     if (qn > 0) drain(qn);
-    if (reg_list) {
-      top = warp_merge_top32(top, warp_sort32_desc(lane < cnt ? my[lane] : 0ull));
-      merged[warp * kp + lane] = lane < K ? top : 0ull;  // kp = 32
-    } else {
-      cnt = warp_prune(my, cnt, K, cap);
-      for (int i = lane; i < kp; i += 32) merged[warp * kp + i] = i < K ? my[i] : 0ull;
-    }
+    if (cnt > 0) list_insert<TWO>(top, warp_sort32_desc(lane < cnt ? my[lane] : 0ull));
+    lists[warp][lane] = top.hi;
+    if (TWO) lists[warp][32 + lane] = top.lo;
     if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&bad_any, 1);
     __syncthreads();
-    if (reg_list) {
-      // the CTA's best 32: warp 0 folds the warps' sorted lists together
-      if (warp == 0) {
-        uint64_t t = merged[lane];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) t = warp_merge_top32(t, merged[w * 32 + lane]);
-        merged[lane] = t;
-        merged[32 + lane] = 0ull;
-        __syncwarp();
-      }
-    } else {
-    // the CTA's best K of the warps' best K: bitonic sort of kWarps * kp keys
-      const int NM = kWarps * kp;
-      for (int kk = 2; kk <= NM; kk <<= 1) {
-        for (int j = kk >> 1; j > 0; j >>= 1) {
-          for (int i = tid; i < NM; i += kThreads) {
-            const int p = i ^ j;
-            if (p > i) {
-              const uint64_t a = merged[i], b = merged[p];
-              const bool desc = (i & kk) == 0;
-              if (desc ? (a < b) : (a > b)) {
-                merged[i] = b;
-                merged[p] = a;
-              }
-            }
-          }
-          __syncthreads();
-        }
-      }
-    }
     if (warp == 0) {
+      // the CTA's best keys: fold the warps' lists together
+      TopList t{lists[0][lane], TWO ? lists[0][32 + lane] : 0ull};
+#pragma unroll 1
+      for (int w = 1; w < kWarps; ++w)
+        list_merge<TWO>(t, TopList{lists[w][lane], TWO ? lists[w][32 + lane] : 0ull});
       // weights of the k best relative to the maximum, then the top-p cut
       FiltRow* fr = recs + row;
       const float sc = P.sc;
-      const uint64_t c0 = merged[lane], c1 = merged[lane + 32];
-      const float xmax = key_value(merged[0]);
+      const uint64_t c0 = t.hi, c1 = TWO ? t.lo : 0ull;
+      const uint64_t best = __shfl_sync(0xffffffffu, c0, 0);
+      const float xmax = key_value(best);
       const float h = xmax * sc;
       const bool v0 = lane < K && c0 != 0ull, v1 = lane + 32 < K && c1 != 0ull;
       const float x0 = v0 ? key_value(c0) : 0.f, x1 = v1 ? key_value(c1) : 0.f;
@@ -467,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
       const bool row_bad = bad_any != 0 || !(xmax > -INFINITY);
       if (lane == 0) {
         fr->n = n;
-        fr->argmax = key_id(merged[0]);
+        fr->argmax = key_id(best);
         fr->h = h;
         fr->z = z;
         fr->xmax = xmax;
@@ -477,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
           float* o = P.out_row_stats + 3 * static_cast<size_t>(row);  // targets, then drafts
           o[0] = xmax / P.T;
           o[1] = z * exp2f(h - xmax * sc);
-          o[2] = __int_as_float(key_id(merged[0]));
+          o[2] = __int_as_float(key_id(best));
         }
       }
     }

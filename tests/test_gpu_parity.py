@@ -371,6 +371,9 @@ FILTERED = [
     (1, 20000, None, 1, 1.0),     # top-1: the argmax only
     (2, 8191, 6, 64, 0.99),       # odd V: rows not 16-byte aligned
     (3, 5003, 40, 20, 0.95),      # ragged lengths
+    (1, 20000, None, 40, 1.0),    # ranks 33..40 in the second register list
+    (2, 8191, 6, 32, 0.9),        # one full register list
+    (2, None, 3, 64, 1.0),        # V = 151,936: many merges into both lists
 ]
 
 
