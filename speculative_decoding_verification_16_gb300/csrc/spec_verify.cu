@@ -159,9 +159,9 @@ int launch_plain(K kernel, const Arg& P, int grid, int threads, int smem, int ma
     int n = 0;
     cudaFuncAttributes fa{};
     cudaError_t e = cudaFuncGetAttributes(&fa, kernel);
-    // kernels that may need more than the default 48 KB: the limit goes to
-    // the device maximum less the kernel's static shared memory
-    if (e == cudaSuccess && smem > 48 * 1024)
+    // kernels that may need more than the default 48 KB (static and dynamic
+    // together): the limit goes to the device maximum less the static part
+    if (e == cudaSuccess && smem + static_cast<int>(fa.sharedSizeBytes) > 48 * 1024)
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                max_smem - static_cast<int>(fa.sharedSizeBytes));
     if (e != cudaSuccess ||
@@ -362,14 +362,13 @@ int run_rows(const Args& a, bool fuse) {
     const int rows = P.Nt + P.Nd;
     const int grid = std::max(1, std::min(rows, dc.sms * kFilterCtasPerSm));
     const bool two = P.top_k > 32;  // kept lists of 64 keys per warp
-    if (es == 2) {
-      if (two) filter_rows_kernel<2, true><<<grid, kThreads, 0, st>>>(P);
-      else filter_rows_kernel<2, false><<<grid, kThreads, 0, st>>>(P);
-    } else {
-      if (two) filter_rows_kernel<4, true><<<grid, kThreads, 0, st>>>(P);
-      else filter_rows_kernel<4, false><<<grid, kThreads, 0, st>>>(P);
-    }
-    return cudaGetLastError() == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+    constexpr int rb = kFilterRingBytes;
+    const int ms = dc.max_smem_optin;
+    if (es == 2)
+      return two ? launch_plain(filter_rows_kernel<2, true>, P, grid, kFiltThreads, rb, ms, false, st)
+                 : launch_plain(filter_rows_kernel<2, false>, P, grid, kFiltThreads, rb, ms, false, st);
+    return two ? launch_plain(filter_rows_kernel<4, true>, P, grid, kFiltThreads, rb, ms, false, st)
+               : launch_plain(filter_rows_kernel<4, false>, P, grid, kFiltThreads, rb, ms, false, st);
   }
   RowsGeom geo;
   rc = rows_geometry(a.V, a.B, es, dc, &geo);

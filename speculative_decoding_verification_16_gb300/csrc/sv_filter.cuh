@@ -34,12 +34,22 @@
 namespace sv {
 
 constexpr int kMaxK = SV_MAX_FILTER_K;  // 64
-constexpr int kCandCap = 288;           // per-warp candidate buffer (31 left over + 256 new)
-// 16-byte loads each thread keeps in flight while it screens (the row is
-// streamed with plain loads, so this sets the bytes in flight per SM), and
-// the CTAs per SM that the registers then allow
-constexpr int kFilterDepth = 2;
-constexpr int kFilterCtasPerSm = kFilterDepth > 1 ? 4 : 5;
+constexpr int kCandCap = 288;           // per-warp staged keys (31 left over + 256 new)
+constexpr int kQCap = 64;               // per-warp queue of vectors that passed the screen
+// The row streams through shared memory: each warp copies chunks of
+// kFilterChunk 16-byte vectors (cp.async.bulk) into its own ring of
+// kFilterStages stages, so the bytes in flight per SM are set by the ring,
+// not by registers.
+constexpr int kFilterChunk = 256;
+constexpr int kFilterStages = 2;
+constexpr int kFilterCtasPerSm = 2;
+constexpr int kFilterRingBytes = kWarps * kFilterStages * kFilterChunk * 16;
+// kWarps streaming warps and one finisher warp
+constexpr int kFiltThreads = (kWarps + 1) * 32;
+// named barriers (0 is __syncthreads): lists of row parity p complete, and
+// the per-row state of parity p clear again
+constexpr int kBarListsFull = 1;
+constexpr int kBarSetFree = 3;
 
 struct FiltRow {
   int32_t n;       // kept tokens (<= k)
@@ -158,6 +168,7 @@ __device__ __forceinline__ uint64_t list_rank(const TopList& t, int j) {
   return __shfl_sync(0xffffffffu, t.hi, j & 31);
 }
 
+
 // Keys of one queued 16-byte vector (vector index k of the row) that beat the
 // bar `thr`, for one lane (valid: the lane holds an entry); NaN and +inf
 // are flagged, not kept.  Returns how many of the VEC keys beat the bar.
@@ -212,82 +223,240 @@ __device__ __forceinline__ float vecs_max(const uint4 (&v)[N]) {
   return m;
 }
 
-// per-warp queue of vectors that passed the screen: fewer than 32 waiting,
-// plus one iteration's worth
-constexpr int kQCap = 32 + 32 * kFilterDepth;
 
-// filter_rows_kernel: the k best keys of a row, k <= 32 (TWO false) or
-// k <= 64 (TWO true).
+// The finisher warp's part of a row: fold the streaming warps' lists into
+// the CTA's best keys, then the weights of the k best relative to the
+// maximum, the top-p cut and the row's FiltRow record.  flagged: a warp saw
+// a NaN or +inf.
+template <bool TWO>
+__device__ __forceinline__ void finish_row(const Params& P, int32_t row, const uint64_t (*lists)[64],
+                                           bool flagged) {
+  const int lane = threadIdx.x & 31;
+  const int K = P.top_k;
+  FiltRow* recs = reinterpret_cast<FiltRow*>(P.filt);
+  TopList t{lists[0][lane], TWO ? lists[0][32 + lane] : 0ull};
+#pragma unroll 1
+  for (int w = 1; w < kWarps; ++w)
+    list_merge<TWO>(t, TopList{lists[w][lane], TWO ? lists[w][32 + lane] : 0ull});
+  // weights of the k best relative to the maximum, then the top-p cut
+  FiltRow* fr = recs + row;
+  const float sc = P.sc;
+  const uint64_t c0 = t.hi, c1 = TWO ? t.lo : 0ull;
+  const uint64_t best = __shfl_sync(0xffffffffu, c0, 0);
+  const float xmax = key_value(best);
+  const float h = xmax * sc;
+  const bool v0 = lane < K && c0 != 0ull, v1 = lane + 32 < K && c1 != 0ull;
+  const float x0 = v0 ? key_value(c0) : 0.f, x1 = v1 ? key_value(c1) : 0.f;
+  const float w0 = v0 ? ex2(fmaf(x0, sc, -h)) : 0.f;
+  const float w1 = v1 ? ex2(fmaf(x1, sc, -h)) : 0.f;
+  const int navail = __popc(__ballot_sync(0xffffffffu, v0)) + __popc(__ballot_sync(0xffffffffu, v1));
+  // inclusive prefix sums in (value desc, id asc) order: entries 0..31, then 32..63
+  float p0 = w0, p1 = w1;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float a = __shfl_up_sync(0xffffffffu, p0, off);
+    const float b = __shfl_up_sync(0xffffffffu, p1, off);
+    if (lane >= off) p0 += a, p1 += b;
+  }
+  const float half = __shfl_sync(0xffffffffu, p0, 31);
+  p1 += half;
+  const float zk = __shfl_sync(0xffffffffu, p1, 31);  // sum of the k weights
+  int n = navail;
+  if (P.top_p < 1.f) {
+    // shortest prefix whose cumulative probability reaches top_p
+    const unsigned r0 = __ballot_sync(0xffffffffu, v0 && p0 / zk >= P.top_p);
+    const unsigned r1 = __ballot_sync(0xffffffffu, v1 && p1 / zk >= P.top_p);
+    if (r0) n = __ffs(r0);
+    else if (r1) n = 32 + __ffs(r1);
+  }
+  float z = n > 32 ? __shfl_sync(0xffffffffu, p1, (n - 33) & 31)
+                   : __shfl_sync(0xffffffffu, p0, (n - 1) & 31);
+  if (n == 0) z = 0.f;
+  if (lane < n) {
+    fr->ids[lane] = key_id(c0);
+    fr->w[lane] = w0;
+  }
+  if (lane + 32 < n) {
+    fr->ids[lane + 32] = key_id(c1);
+    fr->w[lane + 32] = w1;
+  }
+  const bool row_bad = flagged || !(xmax > -INFINITY);
+  if (lane == 0) {
+    fr->n = n;
+    fr->argmax = key_id(best);
+    fr->h = h;
+    fr->z = z;
+    fr->xmax = xmax;
+    fr->flags = row_bad ? SV_DEVERR_NAN : 0;
+    if (row_bad) raise_error(P, SV_DEVERR_NAN);
+    if (P.out_row_stats != nullptr) {
+      float* o = P.out_row_stats + 3 * static_cast<size_t>(row);  // targets, then drafts
+      o[0] = xmax / P.T;
+      o[1] = z * exp2f(h - xmax * sc);
+      o[2] = __int_as_float(key_id(best));
+    }
+  }
+}
+
+// filter_rows_kernel: the k best keys of each row, k <= 32 (TWO false) or
+// k <= 64 (TWO true), one CTA per row at a time.
 //
-// Each warp streams its vectors (vector warp * 32 + lane, then kThreads on)
-// and screens them against a bar: a key at or below it cannot be among the
-// row's k best.  Vectors that pass wait in a per-warp queue; 32 of them at a
-// time become keys, those above the bar are staged, and staged keys merge 32
-// at a time into the warp's register list of its best keys.  Every bar
-// below is valid because it has at least k keys of the row above it:
+// Eight streaming warps each take chunks warp, warp + 8, ... of the row,
+// copied into the warp's shared-memory ring, and screen them against a bar:
+// a key at or below it cannot be among the row's k best.  A key above the
+// bar goes at once into the warp's register list of its best keys (its k-th
+// best is then a bar itself).  Every bar used is valid because at least k
+// keys of the row lie above it:
 //  - a warp's own k-th best key;
 //  - the m-th largest of the warps' published rank-r keys (r = ceil(k / 8),
 //    m = ceil(k / r)): m warps each hold r keys at or above it, m r >= k
 //    keys in all, and the warps' keys are distinct elements of the row;
-//  - before any list fills (k <= 32), the k-th largest of the maxima of the
-//    warp's first 32 vectors (k distinct elements at or above it).
-// A bar that one warp finds serves the whole CTA through a shared word.
+//  - from the first chunk on, the same two with the lanes' maxima over the
+//    chunk standing in for the list (k-th largest: the warp's own, k <= 32;
+//    r-th largest: the key it publishes).
+// Bars are shared through a word in shared memory.  At the end of the row
+// the streaming warps hand their lists to a ninth, finisher warp and go on
+// with the next row while it folds them and writes the row's record.
 template <int ES, bool TWO>
-__global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel(const Params P) {
+__global__ void __launch_bounds__(kFiltThreads, kFilterCtasPerSm) filter_rows_kernel(const Params P) {
   constexpr int VEC = 16 / ES;
+  constexpr int CH = kFilterChunk, NS = kFilterStages, VPL = CH / 32;
+  extern __shared__ __align__(128) unsigned char ring[];  // [kWarps][NS][CH * 16]: copies
+  // per-row state, two sets (row parity): the streaming warps work on one
+  // row while the finisher still reads the other
+  __shared__ uint64_t lists[2][kWarps][64];  // the warps' lists, at the end of a row
   __shared__ uint64_t cand[kWarps][kCandCap];  // staged keys, per warp
-  __shared__ uint64_t lists[kWarps][64];        // the warps' lists, at the end of a row
   __shared__ __align__(16) uint4 qraw[kWarps][kQCap];  // queued vectors
   __shared__ int32_t qidx[kWarps][kQCap];                // their vector indices
-  __shared__ uint64_t pub[kWarps];  // each warp's key of rank r - 1 (0: fewer than r)
-  __shared__ uint64_t cta_bar;      // the best bar any warp has found
-  __shared__ int bad_any;
+  __shared__ __align__(8) uint64_t full_bar[kWarps][NS];  // one per copy stage
+  __shared__ uint64_t pub[2][kWarps];  // each warp's key of rank r - 1 (0: fewer than r)
+  __shared__ uint64_t cta_bar[2];      // the best bar any warp has found
+  __shared__ int bad_any[2];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
   const int K = P.top_k;
   const int r = (K + kWarps - 1) / kWarps;  // 1..8
   const int m = (K + r - 1) / r;            // <= kWarps
-  FiltRow* recs = reinterpret_cast<FiltRow*>(P.filt);
   const int32_t nrows = P.Nt + P.Nd;
+  if (lane == 0 && warp < kWarps)
+    for (int s = 0; s < NS; ++s) mbar_init(smem_addr(&full_bar[warp][s]), 1);
+  if (tid < 2) {
+    cta_bar[tid] = 0ull;
+    bad_any[tid] = 0;
+  }
+  if (tid < 2 * kWarps) pub[tid / kWarps][tid % kWarps] = 0ull;
+  fence_mbar_init();
+  __syncthreads();
   grid_dep_launch_dependents();
 
-  for (int32_t row = blockIdx.x; row < nrows; row += gridDim.x) {
-    const bool is_t = row < P.Nt;
-    const unsigned char* base =
-        is_t ? P.tgt + static_cast<size_t>(row) * P.V * ES
-             : P.drf + static_cast<size_t>(row - P.Nt) * P.V * ES;
-    const Slice s = make_slice<ES>(base, P.V, 0, P.V);  // the whole row
+  if (warp == kWarps) {
+    // the finisher: row t's lists are complete once every streaming warp has
+    // arrived on kBarListsFull + (t & 1); it then clears that set for the
+    // CTA's row t + 2 and releases it on kBarSetFree + (t & 1)
+    int t = 0;
+    for (int32_t row = blockIdx.x; row < nrows; row += gridDim.x, ++t) {
+      const int b = t & 1;
+      named_bar_sync(kBarListsFull + b, kFiltThreads);
+      finish_row<TWO>(P, row, lists[b], bad_any[b] != 0);
+      if (row + 2 * static_cast<int32_t>(gridDim.x) < nrows) {
+        if (lane < kWarps) pub[b][lane] = 0ull;
+        if (lane == 0) {
+          cta_bar[b] = 0ull;
+          bad_any[b] = 0;
+        }
+        __threadfence_block();
+        named_bar_arrive(kBarSetFree + b, kFiltThreads);
+      }
+    }
+    return;
+  }
+  unsigned char* my_ring = ring + warp * NS * CH * 16;
+
+  auto row_slice = [&](int32_t row) {
+    const unsigned char* base = row < P.Nt ? P.tgt + static_cast<size_t>(row) * P.V * ES
+                                           : P.drf + static_cast<size_t>(row - P.Nt) * P.V * ES;
+    return make_slice<ES>(base, P.V, 0, P.V);  // the whole row
+  };
+  // chunks (CH vectors, the last one shorter) of a row of nv vectors that
+  // this warp takes: warp, warp + kWarps, ...
+  auto warp_chunks = [&](int32_t nv) {
+    const int32_t nch = (nv + CH - 1) / CH;
+    return nch > warp ? (nch - warp + kWarps - 1) / kWarps : 0;
+  };
+
+  // The warp's copies form one stream over the CTA's rows: lane 0 keeps NS
+  // of them in flight and, each time the warp has read a stage, refills it
+  // with the next chunk of the stream (the next row's, near a row's end).
+  int32_t p_row = blockIdx.x, p_i = 0, p_nch = 0, p_nbytes = 0;
+  const unsigned char* p_src = nullptr;
+  uint32_t pseq = 0, cseq = 0;  // copies issued / consumed by this warp
+  bool timed_out = false;       // a copy never arrived: stop issuing, skip work
+  auto p_open = [&]() {         // the first row from p_row on with a chunk for this warp
+    for (; p_row < nrows; p_row += gridDim.x) {
+      const Slice ps = row_slice(p_row);
+      p_nch = warp_chunks(ps.nbytes >> 4);
+      if (p_nch > 0) {
+        p_src = ps.gsrc;
+        p_nbytes = ps.nbytes;
+        p_i = 0;
+        return;
+      }
+    }
+  };
+  auto issue = [&]() {
+    if (p_row >= nrows || timed_out) return;
+    const int32_t off = (warp + kWarps * p_i) * CH * 16;
+    const uint32_t bytes = static_cast<uint32_t>(min(CH * 16, p_nbytes - off));  // 16 | bytes
+    const int stg = static_cast<int>(pseq % NS);
+    if (lane == 0) {
+      const uint32_t bar = smem_addr(&full_bar[warp][stg]);
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_g2s(smem_addr(my_ring + stg * CH * 16), p_src + off, bytes, bar);
+    }
+    ++pseq;
+    if (++p_i == p_nch) {
+      p_row += gridDim.x;
+      p_open();
+    }
+  };
+  p_open();
+  for (int s = 0; s < NS; ++s) issue();
+
+  int t = 0;
+  for (int32_t row = blockIdx.x; row < nrows; row += gridDim.x, ++t) {
+    const int b = t & 1;
+    if (t >= 2) named_bar_sync(kBarSetFree + b, kFiltThreads);  // set b is clear again
+    const Slice s = row_slice(row);
     const int32_t nv = s.nbytes >> 4;
     uint64_t* my = cand[warp];
-    if (tid == 0) {
-      bad_any = 0;
-      cta_bar = 0ull;
-    }
-    if (tid < kWarps) pub[tid] = 0ull;
-    __syncthreads();
     int cnt = 0;                // warp-uniform: staged keys
+    int qn = 0;                 // warp-uniform: vectors waiting in the warp's queue
+    uint64_t pubv = 0;          // warp-uniform: this warp's published key
     uint64_t thr = 0;           // warp-uniform: the bar
     float thr_val = -INFINITY;  // the logit of that key (the screen's bar)
     bool bad = false;
-    int qn = 0;                 // warp-uniform: vectors waiting in the warp's queue
     TopList top{0ull, 0ull};
 
-    // adopt a bar (warp-uniform) and share it
+    // adopt a bar (warp-uniform) and share it with the CTA
     auto raise_to = [&](uint64_t nb) {
       if (nb > thr) {
         thr = nb;
         thr_val = key_value(nb);
-        if (lane == 0) atomicMax(reinterpret_cast<unsigned long long*>(&cta_bar), nb);
+        if (lane == 0) atomicMax(reinterpret_cast<unsigned long long*>(&cta_bar[b]), nb);
       }
     };
-    // after the list changed: the warp's k-th best key, and the m-th largest
-    // of the published rank-r keys (this warp's own just updated)
-    auto list_bars = [&]() {
-      const uint64_t own = list_rank<TWO>(top, K - 1);
-      const uint64_t mine = list_rank<TWO>(top, r - 1);
-      if (lane == 0) pub[warp] = mine;
+    // publish a key with at least r of this warp's elements at or above it
+    // (the largest so far: every one published stays true)
+    auto publish = [&](uint64_t key) {
+      if (key > pubv) {
+        pubv = key;
+        if (lane == 0) pub[b][warp] = key;
+      }
+    };
+    // the m-th largest of the warps' published keys, less one
+    auto cta_combined = [&]() {
       __syncwarp();
-      const uint64_t v = lane < kWarps ? *reinterpret_cast<volatile uint64_t*>(&pub[lane]) : 0ull;
+      const uint64_t v = lane < kWarps ? *reinterpret_cast<volatile uint64_t*>(&pub[b][lane]) : 0ull;
       int gt = 0, ge = 0;
 #pragma unroll
       for (int j = 0; j < kWarps; ++j) {
@@ -297,8 +466,14 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
       }
       const unsigned sel = __ballot_sync(0xffffffffu, lane < kWarps && gt < m && m <= ge);
       const uint64_t q = sel ? __shfl_sync(0xffffffffu, v, __ffs(sel) - 1) : 0ull;
-      const uint64_t qb = q > 0ull ? q - 1ull : 0ull;
-      raise_to(own > qb ? own : qb);
+      if (q > 0ull) raise_to(q - 1ull);
+    };
+    // after the list changed: the warp's k-th best key, its rank-r key
+    // published, and the combination
+    auto list_bars = [&]() {
+      raise_to(list_rank<TWO>(top, K - 1));
+      publish(list_rank<TWO>(top, r - 1));
+      cta_combined();
     };
 
     // Keys of the first n queued vectors (lane l takes entry l) that beat
@@ -335,167 +510,104 @@ __global__ void __launch_bounds__(kThreads, kFilterCtasPerSm) filter_rows_kernel
       list_bars();
     };
 
-    // The warp's vectors are k0 + j kThreads, j = 0, 1, ... (step j).  Each
-    // iteration screens kFilterDepth steps while the loads of the next
-    // kFilterDepth are in flight (clamped into the row, so that no load needs
-    // a branch; a clamped copy is never queued as a row element).
-    const int32_t k0 = warp * 32 + lane;
-    const int32_t rem = nv - warp * 32;
-    const int32_t nsteps = rem > 0 ? (rem - 1) / kThreads + 1 : 0;
-    auto load_step = [&](int32_t j) {
-      const int32_t k = min(k0 + j * kThreads, nv - 1);
-      return ldg_nc_v4(s.gsrc + 16 * static_cast<size_t>(k));
-    };
-    uint4 nxt[kFilterDepth];
+    const int32_t mych = timed_out ? 0 : warp_chunks(nv);
+    for (int32_t i = 0; i < mych; ++i) {
+      const int stg = static_cast<int>(cseq % NS);
+      mbar_wait(smem_addr(&full_bar[warp][stg]), (cseq / NS) & 1u, timed_out);
+      timed_out = __any_sync(0xffffffffu, timed_out);  // lanes may see the limit apart
+      if (timed_out) break;
+      const int32_t kbase = (warp + kWarps * i) * CH;  // the chunk's first vector
+      const unsigned char* buf = my_ring + stg * CH * 16;
+      uint4 v[VPL];  // lane's vectors kbase + lane + 32 t (stale past the row's end)
 #pragma unroll
-    for (int d = 0; d < kFilterDepth; ++d) nxt[d] = load_step(d);
-    if (!TWO) {
-      // the first bar: just below the k-th largest of the lanes' first-vector
-      // maximum keys (so that the maximum itself still passes; the low half
-      // of a key, a complemented id, is never zero)
-      uint64_t key[VEC];
-      bool seed_bad = false;
-      vector_keys<ES>(nxt[0], k0, k0 < nv, s, 0ull, key, seed_bad);
-      uint64_t mk = key[0];
-#pragma unroll
-      for (int l = 1; l < VEC; ++l) mk = max(mk, key[l]);
-      int above = 0;  // lanes whose maximum key is larger than this lane's
+      for (int t = 0; t < VPL; ++t) v[t] = *reinterpret_cast<const uint4*>(buf + 16 * (lane + 32 * t));
+      const float vm = vecs_max<ES, VPL>(v);
+      if (i == 0 && kbase + CH <= nv) {
+        // first bars from the lanes' maxima over this chunk (NaN maxima
+        // count as -inf): with x the j-th largest of them, j distinct
+        // elements have values at or above x, so their keys are at or above
+        // order_key(x) << 32.  j = k gives this warp's own bar (k <= 32),
+        // j = r the key it publishes.
+        const float mx = vm == vm ? vm : -INFINITY;
+        int gt = 0, ge = 0;
 #pragma unroll 8
-      for (int o = 0; o < 32; ++o) above += __shfl_sync(0xffffffffu, mk, o) > mk;
-      // keys are unique; lanes past the row hold 0, which never seeds
-      const unsigned rk = __ballot_sync(0xffffffffu, above == K - 1 && mk != 0ull);
-      if (rk) raise_to(__shfl_sync(0xffffffffu, mk, __ffs(rk) - 1) - 1ull);
-    }
-    for (int32_t j = 0; j < nsteps; j += kFilterDepth) {
-      uint4 cur[kFilterDepth];
-#pragma unroll
-      for (int d = 0; d < kFilterDepth; ++d) {
-        cur[d] = nxt[d];
-        nxt[d] = load_step(j + kFilterDepth + d);
+        for (int o = 0; o < 32; ++o) {
+          const float y = __shfl_sync(0xffffffffu, mx, o);
+          gt += y > mx;
+          ge += y >= mx;
+        }
+        if (!TWO) {
+          const unsigned sk = __ballot_sync(0xffffffffu, gt < K && K <= ge);
+          const float x = __shfl_sync(0xffffffffu, mx, sk ? __ffs(sk) - 1 : 0);
+          if (sk && x > -INFINITY) raise_to((static_cast<uint64_t>(order_key(x)) << 32) - 1ull);
+        }
+        const unsigned sr = __ballot_sync(0xffffffffu, gt < r && r <= ge);
+        const float xr = __shfl_sync(0xffffffffu, mx, sr ? __ffs(sr) - 1 : 0);
+        if (sr && xr > -INFINITY) publish(static_cast<uint64_t>(order_key(xr)) << 32);
       }
       // the best bar any warp has found (a stale one only lets more through)
-      const uint64_t cb = *reinterpret_cast<volatile uint64_t*>(&cta_bar);
+      const uint64_t cb = *reinterpret_cast<volatile uint64_t*>(&cta_bar[b]);
       if (cb > thr) {
         thr = cb;
         thr_val = key_value(cb);
       }
-      // screen: no logit of these vectors reaches the bar (clamped copies
-      // past the row only make the test pass more often)
-      if (__ballot_sync(0xffffffffu, !(vecs_max<ES, kFilterDepth>(cur) < thr_val)) == 0) continue;
-      // queue each vector whose largest logit is not below the bar (a NaN
-      // maximum is queued and flagged by the drain)
-#pragma unroll
-      for (int d = 0; d < kFilterDepth; ++d) {
-        const int32_t k = k0 + (j + d) * kThreads;
-        const bool maybe = k < nv && !(vec_max<ES>(cur[d]) < thr_val);
-        const unsigned mq = __ballot_sync(0xffffffffu, maybe);
-        if (maybe) {
-          const int at = qn + __popc(mq & lt_mask);
-          qraw[warp][at] = cur[d];
-          qidx[warp][at] = k;
-        }
-        qn += __popc(mq);
-      }
-      __syncwarp();
-      while (qn >= 32) {
-        drain(32);
-        // move the rest (fewer than 32 kFilterDepth) to the front
-        const int rest = qn - 32;
-        uint4 r4[kFilterDepth];
-        int32_t ri[kFilterDepth];
-#pragma unroll
-        for (int t = 0; t < kFilterDepth; ++t) {
-          const int i = lane + 32 * t;
-          if (i < rest) {
-            r4[t] = qraw[warp][32 + i];
-            ri[t] = qidx[warp][32 + i];
+      // screen: no logit of the chunk reaches the bar (stale entries past the
+      // row's end only make the test pass more often)
+      if (__ballot_sync(0xffffffffu, !(vm < thr_val)) != 0) {
+        // queue each vector whose largest logit is not below the bar (a NaN
+        // maximum is queued and flagged by the drain)
+#pragma unroll 1
+        for (int t = 0; t < VPL; ++t) {
+          const int32_t k = kbase + lane + 32 * t;
+          const uint4 raw = *reinterpret_cast<const uint4*>(buf + 16 * (lane + 32 * t));
+          const bool maybe = k < nv && !(vec_max<ES>(raw) < thr_val);
+          const unsigned mq = __ballot_sync(0xffffffffu, maybe);
+          if (maybe) {
+            const int at = qn + __popc(mq & lt_mask);
+            qraw[warp][at] = raw;
+            qidx[warp][at] = k;
+          }
+          qn += __popc(mq);
+          __syncwarp();
+          if (qn >= 32) {
+            drain(32);
+            // move the rest (at most 31) to the front
+            const int rest = qn - 32;
+            uint4 r4;
+            int32_t ri = 0;
+            if (lane < rest) {
+              r4 = qraw[warp][32 + lane];
+              ri = qidx[warp][32 + lane];
+            }
+            __syncwarp();
+            if (lane < rest) {
+              qraw[warp][lane] = r4;
+              qidx[warp][lane] = ri;
+            }
+            __syncwarp();
+            qn = rest;
           }
         }
-        __syncwarp();
-#pragma unroll
-        for (int t = 0; t < kFilterDepth; ++t) {
-          const int i = lane + 32 * t;
-          if (i < rest) {
-            qraw[warp][i] = r4[t];
-            qidx[warp][i] = ri[t];
-          }
-        }
-        __syncwarp();
-        qn = rest;
       }
+      __syncwarp();  // every lane has read the stage: refill it
+      ++cseq;
+      issue();
     }
     if (qn > 0) drain(qn);
     if (cnt > 0) list_insert<TWO>(top, warp_sort32_desc(lane < cnt ? my[lane] : 0ull));
-    lists[warp][lane] = top.hi;
-    if (TWO) lists[warp][32 + lane] = top.lo;
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&bad_any, 1);
-    __syncthreads();
-    if (warp == 0) {
-      // the CTA's best keys: fold the warps' lists together
-      TopList t{lists[0][lane], TWO ? lists[0][32 + lane] : 0ull};
-#pragma unroll 1
-      for (int w = 1; w < kWarps; ++w)
-        list_merge<TWO>(t, TopList{lists[w][lane], TWO ? lists[w][32 + lane] : 0ull});
-      // weights of the k best relative to the maximum, then the top-p cut
-      FiltRow* fr = recs + row;
-      const float sc = P.sc;
-      const uint64_t c0 = t.hi, c1 = TWO ? t.lo : 0ull;
-      const uint64_t best = __shfl_sync(0xffffffffu, c0, 0);
-      const float xmax = key_value(best);
-      const float h = xmax * sc;
-      const bool v0 = lane < K && c0 != 0ull, v1 = lane + 32 < K && c1 != 0ull;
-      const float x0 = v0 ? key_value(c0) : 0.f, x1 = v1 ? key_value(c1) : 0.f;
-      const float w0 = v0 ? ex2(fmaf(x0, sc, -h)) : 0.f;
-      const float w1 = v1 ? ex2(fmaf(x1, sc, -h)) : 0.f;
-      const int navail = __popc(__ballot_sync(0xffffffffu, v0)) + __popc(__ballot_sync(0xffffffffu, v1));
-      // inclusive prefix sums in (value desc, id asc) order: entries 0..31, then 32..63
-      float p0 = w0, p1 = w1;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float a = __shfl_up_sync(0xffffffffu, p0, off);
-        const float b = __shfl_up_sync(0xffffffffu, p1, off);
-        if (lane >= off) p0 += a, p1 += b;
-      }
-      const float half = __shfl_sync(0xffffffffu, p0, 31);
-      p1 += half;
-      const float zk = __shfl_sync(0xffffffffu, p1, 31);  // sum of the k weights
-      int n = navail;
-      if (P.top_p < 1.f) {
-        // shortest prefix whose cumulative probability reaches top_p
-        const unsigned r0 = __ballot_sync(0xffffffffu, v0 && p0 / zk >= P.top_p);
-        const unsigned r1 = __ballot_sync(0xffffffffu, v1 && p1 / zk >= P.top_p);
-        if (r0) n = __ffs(r0);
-        else if (r1) n = 32 + __ffs(r1);
-      }
-      float z = n > 32 ? __shfl_sync(0xffffffffu, p1, (n - 33) & 31)
-                       : __shfl_sync(0xffffffffu, p0, (n - 1) & 31);
-      if (n == 0) z = 0.f;
-      if (lane < n) {
-        fr->ids[lane] = key_id(c0);
-        fr->w[lane] = w0;
-      }
-      if (lane + 32 < n) {
-        fr->ids[lane + 32] = key_id(c1);
-        fr->w[lane + 32] = w1;
-      }
-      const bool row_bad = bad_any != 0 || !(xmax > -INFINITY);
-      if (lane == 0) {
-        fr->n = n;
-        fr->argmax = key_id(best);
-        fr->h = h;
-        fr->z = z;
-        fr->xmax = xmax;
-        fr->flags = row_bad ? SV_DEVERR_NAN : 0;
-        if (row_bad) raise_error(P, SV_DEVERR_NAN);
-        if (P.out_row_stats != nullptr) {
-          float* o = P.out_row_stats + 3 * static_cast<size_t>(row);  // targets, then drafts
-          o[0] = xmax / P.T;
-          o[1] = z * exp2f(h - xmax * sc);
-          o[2] = __int_as_float(key_id(best));
-        }
-      }
-    }
-    __syncthreads();
+    lists[b][warp][lane] = top.hi;
+    if (TWO) lists[b][warp][32 + lane] = top.lo;
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&bad_any[b], 1);
+    __threadfence_block();
+    named_bar_arrive(kBarListsFull + b, kFiltThreads);  // the lists go to the finisher
+  }
+  if (timed_out) {
+    // a copy did not arrive in time: report it, and before the CTA exits
+    // wait (bounded) for every copy still in flight into its shared memory
+    if (lane == 0) raise_error(P, SV_DEVERR_TIMEOUT);
+    bool again = false;
+    for (; cseq < pseq; ++cseq)
+      mbar_wait(smem_addr(&full_bar[warp][cseq % NS]), (cseq / NS) & 1u, again);
   }
 }
 

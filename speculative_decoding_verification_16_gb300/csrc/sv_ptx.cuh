@@ -33,6 +33,18 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// Named CTA barriers (id 1..15; count: threads taking part, a multiple of
+// 32).  sync waits for the barrier; arrive only counts this warp in.  Both
+// order the calling threads' earlier shared-memory accesses before the
+// threads that then pass the barrier.
+__device__ __forceinline__ void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void named_bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // One wait attempt.  The hint lets the hardware suspend the thread (instead
 // of spinning on the issue slot) until the phase completes or ~0.5 ms pass.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {

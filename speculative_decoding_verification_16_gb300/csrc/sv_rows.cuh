@@ -524,10 +524,6 @@ __device__ __forceinline__ void st_relaxed_u64(uint64_t* p, uint64_t v) {
 }
 
 
-__device__ __forceinline__ void named_bar_sync(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // Threads of the rows kernel: NCW consumer warps, producer, publishers, gatherers.
 __host__ __device__ constexpr int rows_threads(int ncw) { return (ncw + 1 + kPublishers + kGatherers) * 32; }
 
