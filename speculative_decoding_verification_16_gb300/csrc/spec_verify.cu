@@ -394,8 +394,13 @@ int run_rows(const Args& a, bool fuse) {
   const bool track = a.mode == SV_GREEDY || a.out_row_stats != nullptr;
   // consumer warps (16 or 24) and, with labels, how many of them run pass 1
   // (SV_TUNE_WARPS, SV_TUNE_PASS1_WARPS)
+  // Default split: half the warps on pass 1; with the exact max / argmax
+  // tracked (greedy, statistics) pass 1 carries about a third more work, and
+  // 11 of 16 warps on it measured fastest (conc32 greedy with labels: 97 us
+  // against 106 us at 8).
   const int ncw = tu.warps >= 24 ? 24 : 16;
-  P.nw1 = std::max(1, std::min(ncw - 1, tu.pass1_warps > 0 ? tu.pass1_warps : ncw / 2));
+  const int dflt1 = track && ncw == 16 ? 11 : ncw / 2;
+  P.nw1 = std::max(1, std::min(ncw - 1, tu.pass1_warps > 0 ? tu.pass1_warps : dflt1));
   if (es == 2)
     return ncw == 24 ? launch_rows<2, 24>(P, smem, dc, need_z, need_conf, track, st)
                      : launch_rows<2, 16>(P, smem, dc, need_z, need_conf, track, st);
@@ -420,8 +425,8 @@ int run_finalize(const Args& a, bool after_rows) {
     return launch_plain(gfilter_requests_kernel<4>, P, a.B, kGThreads, 0, dc.max_smem_optin,
                         after_rows, st);
   }
-  if (P.top_k > 0)  // top-k / top-p: decisions on the kept sets, one warp per request
-    return launch_plain(filter_requests_kernel, P, per_warp_grid, kThreads, 0, dc.max_smem_optin,
+  if (P.top_k > 0)  // top-k / top-p: decisions on the kept sets, one CTA per request
+    return launch_plain(filter_requests_kernel, P, a.B, kReqWarps * 32, 0, dc.max_smem_optin,
                         after_rows, st);
   RowsGeom geo;
   rc = rows_geometry(a.V, a.B, es, dc, &geo);

@@ -625,35 +625,44 @@ __device__ __forceinline__ void copy_row(FiltRow& dst, const FiltRow* src, int l
   __syncwarp();
 }
 
-// One warp per request: accept chain, labels, final token, outputs.
-__global__ void __launch_bounds__(kThreads) filter_requests_kernel(const Params P) {
-  __shared__ FiltRow rows[kWarps][2];  // target row, draft row of the current position
-  __shared__ int32_t draw_id[kWarps][kMaxK];
-  __shared__ float draw_w[kWarps][kMaxK];
+// filter_requests_kernel: one CTA per request, kReqWarps warps.  Warp w
+// takes drafted positions w, w + kReqWarps, ...: it copies the pair of row
+// records, writes the label and records a rejection (the first one is
+// kept); warp 0 then draws the final token from the rows of the first
+// rejected position (or the bonus row) and writes the outputs.
+constexpr int kReqWarps = 16;
+
+__global__ void __launch_bounds__(kReqWarps * 32) filter_requests_kernel(const Params P) {
+  __shared__ FiltRow rows[kReqWarps][2];  // per warp: target row, draft row of its position
+  __shared__ int32_t draw_id[kMaxK];
+  __shared__ float draw_w[kMaxK];
+  __shared__ int32_t fail_pos;  // first rejected drafted position, or l - 1
+  __shared__ int flags_sh;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int32_t r = blockIdx.x * kWarps + warp;
-  if (r >= P.B) return;  // whole warps leave together
+  const int32_t r = blockIdx.x;
   const FiltRow* recs = reinterpret_cast<const FiltRow*>(P.filt);
-  FiltRow& T = rows[warp][0];
-  FiltRow& D = rows[warp][1];
   const int32_t off = __ldg(P.offs + r), off1 = __ldg(P.offs + r + 1), ell = __ldg(P.lens + r);
   const bool ok = ell >= 1 && ell <= P.max_len && off1 - off == ell && off >= r && off1 <= P.Nt &&
                   (r != 0 || off == 0) && (r != P.B - 1 || off1 == P.Nt) &&
                   off - r + ell - 1 <= P.Nd;
-  if (!ok) {
-    if (lane == 0) raise_error(P, SV_DEVERR_LEN);
+  if (!ok) {  // uniform over the CTA
+    if (threadIdx.x == 0) raise_error(P, SV_DEVERR_LEN);
     return;
   }
+  if (threadIdx.x == 0) {
+    fail_pos = ell - 1;
+    flags_sh = 0;
+  }
   grid_dep_wait();  // the row records come from filter_rows_kernel
+  __syncthreads();
+  FiltRow& T = rows[warp][0];
+  FiltRow& D = rows[warp][1];
   int flags = 0;
-  // labels of every drafted position, and the accept chain up to the first failure
-  int32_t a = ell - 1;
-  bool stopped = false;
-  for (int32_t j = 0; j < ell - 1; ++j) {
+  // labels of every drafted position, and the accept tests
+  for (int32_t j = warp; j < ell - 1; j += kReqWarps) {
     copy_row(T, recs + off + j, lane);
     copy_row(D, recs + P.Nt + off - r + j, lane);
     if (lane == 0) flags |= T.flags | D.flags;
-    const int32_t x = __ldg(P.draft_tokens + off - r + j);
     if (P.out_conf != nullptr) {
       float c = 0.f;
       for (int i = lane; i < T.n; i += 32) c += fminf(T.w[i] / T.z, kept_prob(D, T.ids[i]));
@@ -661,24 +670,28 @@ __global__ void __launch_bounds__(kThreads) filter_requests_kernel(const Params 
       for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
       if (lane == 0) P.out_conf[off - r + j] = c;
     }
-    if (stopped) continue;
-    bool acc;
-    if (x < 0 || x >= P.V) {
-      flags |= SV_DEVERR_TOKEN;
-      acc = false;
-    } else if (P.mode == SV_GREEDY) {
-      acc = x == T.argmax;
-    } else {
-      const float pt = kept_prob(T, x), pd = kept_prob(D, x);
-      const float u = __ldg(P.uniforms + off + j);
-      acc = pd > 0.f ? u * pd < pt : pt > 0.f;
+    if (lane == 0) {
+      const int32_t x = __ldg(P.draft_tokens + off - r + j);
+      bool acc;
+      if (x < 0 || x >= P.V) {
+        flags |= SV_DEVERR_TOKEN;
+        acc = false;
+      } else if (P.mode == SV_GREEDY) {
+        acc = x == T.argmax;
+      } else {
+        const float pt = kept_prob(T, x), pd = kept_prob(D, x);
+        const float u = __ldg(P.uniforms + off + j);
+        acc = pd > 0.f ? u * pd < pt : pt > 0.f;
+      }
+      if (!acc) atomicMin(&fail_pos, j);
     }
-    if (!acc) {
-      a = j;
-      stopped = true;
-      if (P.out_conf == nullptr) break;
-    }
+    __syncwarp();  // the warp's row slots are reused for its next position
   }
+  if (lane == 0 && flags) atomicOr(&flags_sh, flags);
+  __syncthreads();
+  if (warp != 0) return;
+  const int32_t a = fail_pos;
+  flags = 0;
   // final token from target row a (and its draft partner when a < l - 1)
   copy_row(T, recs + off + a, lane);
   if (lane == 0) flags |= T.flags;
@@ -687,8 +700,8 @@ __global__ void __launch_bounds__(kThreads) filter_requests_kernel(const Params 
     const bool residual = a < ell - 1;
     if (residual) copy_row(D, recs + P.Nt + off - r + a, lane);
     // weights of the kept target tokens, then sorted by id (ascending)
-    int32_t* sid = draw_id[warp];
-    float* swt = draw_w[warp];
+    int32_t* sid = draw_id;
+    float* swt = draw_w;
     float tot = 0.f;
     for (int q = 0; q < 2; ++q) {
       const int i = lane + 32 * q;
@@ -762,6 +775,7 @@ __global__ void __launch_bounds__(kThreads) filter_requests_kernel(const Params 
   flags = __reduce_or_sync(0xffffffffu, flags);
   if (lane == 0) {
     P.out_accept_len[r] = a;
+    flags |= flags_sh;
     if (flags) raise_error(P, flags);
   }
 }
