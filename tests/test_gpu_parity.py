@@ -86,7 +86,7 @@ def test_small_workloads_every_request(cuda_lib, idx, V, B, lens, L, mode):
 @pytest.mark.parametrize("idx,mode,sample", [
     (1, W.SAMPLE, None), (1, W.GREEDY, None),
     (2, W.SAMPLE, None), (2, W.GREEDY, None),
-    (3, W.SAMPLE, 40),
+    (3, W.SAMPLE, None),
 ])
 def test_full_size_workloads(cuda_lib, idx, mode, sample):
     """Full sizes in the launch configuration the bench times; the oracle
@@ -389,11 +389,11 @@ def test_filtered_every_request(cuda_lib, idx, V, B, top_k, top_p, mode):
 
 
 def test_filtered_full_size_workload(cuda_lib):
-    """B=512 requests of block 16, V=262,144 bf16, top_k 20, top_p 0.95: every
-    request's outputs against the oracle on a sample of 16 requests."""
+    """B=512 requests of block 16, V=262,144 bf16, top_k 20, top_p 0.95: the
+    outputs of one call against the oracle on a seeded sample of 48 requests."""
     spec = W.WORKLOADS[4]
     w = W.make_workload(spec, W.SAMPLE, seed=43, device=DEV)
-    reqs = sorted(np.random.default_rng(5).choice(w.B, 16, replace=False).tolist())
+    reqs = sorted(np.random.default_rng(5).choice(w.B, 48, replace=False).tolist())
     run_and_compare(cuda_lib, w, requests=reqs, want_stats=True)
 
 
