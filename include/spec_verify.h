@@ -127,7 +127,7 @@ size_t spec_verify_workspace_size(int32_t B, int32_t n_target_rows);
  *  top_p          in (0, 1]; 1 = off.  Filtered calls whose kept set is at
  *                 most SV_MAX_FILTER_K tokens (top_k <= 64 on) run the small
  *                 kept-set path: one pass per row selects the set exactly,
- *                 then one warp per request decides on it.  Larger kept
+ *                 then one CTA per request decides on it.  Larger kept
  *                 sets (top_k above 64, or top_p over the whole vocabulary)
  *                 run the general path: per row a search over weight bins
  *                 and key digits with exact fixed-point mass sums finds the

@@ -12,7 +12,8 @@
 //                       prefix of that order whose cumulative probability
 //                       reaches top_p), renormalised again.  The kept tokens
 //                       and weights go to a FiltRow record in the workspace.
-//  filter_requests_kernel  one warp per request, on the FiltRow records only:
+//  filter_requests_kernel  one CTA per request, a warp per drafted
+//                       position, on the FiltRow records only:
 //                       the accept chain u * p_d(x) < p_t(x) (greedy: x is
 //                       the target argmax), the confidence labels
 //                       c* = sum_v min(p_t, p_d) over the two kept sets
