@@ -276,6 +276,7 @@ int spec_verify_schedule(const float* conf, int32_t B, int32_t K, const double* 
  *                        0 or default: half, or 12 of 16 when the exact
  *                        row maximum is tracked (greedy, row statistics)
  *   SV_TUNE_POLL_NS      sleep between polls of another CTA's words, 0..10000
+ *                        (default 64 ns)
  *   SV_TUNE_XWAIT_NS     limit of a wait on words that other CTAs of the
  *                        same launch publish, 0..200000000 (default 200 ms);
  *                        a wait that reaches it gives up, the call raises

@@ -43,7 +43,8 @@ struct Tuning {
   int stages = kMaxStages;  // most shared-memory stages
   int warps = 16;           // consumer warps (16 or 24)
   int pass1_warps = 0;      // consumer warps on pass 1 with labels on; 0: half
-  int poll_ns = 128;        // sleep between polls of another CTA's words
+  int poll_ns = 64;         // sleep between polls of another CTA's words (64 ns: ~1 %
+                            // faster than 128 on conc32 sampling, greedy unchanged)
   int64_t xwait_ns = static_cast<int64_t>(kWaitLimitNs);  // limit of a wait on other CTAs
 };
 std::mutex g_tune_mu;
