@@ -603,8 +603,19 @@ def run_e2e(L, w, spec, mode, dev, stream, kw, K, world):
     torch.cuda.synchronize(dev)
     ms = max_over_ranks(a.elapsed_time(b), world, dev)
     value = sum_over_ranks(steps * w.n_draft_rows, world, dev) / (ms / 1e3)
+    # the bound: one step's upload alone (pinned host -> device, copy stream)
+    torch.cuda.synchronize(dev)
+    ua, ub = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ua.record(copy_stream)
+    for i in range(3):
+        upload(i)
+    ub.record(copy_stream)
+    torch.cuda.synchronize(dev)
+    up_ms = ua.elapsed_time(ub) / 3
     return {"value": value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "overlap": "next step's upload during this step's verify"}
+            "steps": steps, "overlap": "next step's upload during this step's verify",
+            "h2d_gbs_in_loop": h2d * steps / (ms / 1e3) / 1e9,
+            "h2d_gbs_upload_alone": h2d / (up_ms / 1e3) / 1e9}
 
 
 def run_schedule(args, rank):
