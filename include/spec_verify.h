@@ -273,7 +273,7 @@ int spec_verify_schedule(const float* conf, int32_t B, int32_t K, const double* 
  *   SV_TUNE_STAGES       most shared-memory stages, 4..6
  *   SV_TUNE_WARPS        consumer warps, 16 or 24
  *   SV_TUNE_PASS1_WARPS  consumer warps on pass 1 when labels are on, 0 .. 23;
- *                        0 or default: half, or 12 of 16 when the exact
+ *                        0 or default: half, or 11 of 16 when the exact
  *                        row maximum is tracked (greedy, row statistics)
  *   SV_TUNE_POLL_NS      sleep between polls of another CTA's words, 0..10000
  *                        (default 64 ns)

@@ -397,10 +397,10 @@ int run_rows(const Args& a, bool fuse) {
   // (SV_TUNE_WARPS, SV_TUNE_PASS1_WARPS)
   // Default split: half the warps on pass 1; with the exact max / argmax
   // tracked (greedy, statistics) pass 1 carries about a third more work, and
-  // 12 of 16 warps on it (two subgroups of 6) measured fastest (conc32
-  // greedy with labels: 94 us against 108 us at 8).
+  // 11 of 16 warps on it measured fastest (conc32 greedy with labels: 97 us
+  // against 106 us at 8).
   const int ncw = tu.warps >= 24 ? 24 : 16;
-  const int dflt1 = track && ncw == 16 ? 12 : ncw / 2;
+  const int dflt1 = track && ncw == 16 ? 11 : ncw / 2;
   P.nw1 = std::max(1, std::min(ncw - 1, tu.pass1_warps > 0 ? tu.pass1_warps : dflt1));
   if (es == 2)
     return ncw == 24 ? launch_rows<2, 24>(P, smem, dc, need_z, need_conf, track, st)

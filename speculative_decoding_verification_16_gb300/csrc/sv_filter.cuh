@@ -82,15 +82,6 @@ __device__ __forceinline__ int32_t key_id(uint64_t c) {
   return static_cast<int32_t>(~static_cast<uint32_t>(c));
 }
 
-// 16-byte read-only load that does not allocate in L1.
-__device__ __forceinline__ uint4 ldg_nc_v4(const unsigned char* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // Descending bitonic sort of one key per lane across the warp.
 __device__ __forceinline__ uint64_t warp_sort32_desc(uint64_t v) {
   const int lane = threadIdx.x & 31;
@@ -304,10 +295,11 @@ __device__ __forceinline__ void finish_row(const Params& P, int32_t row, const u
 //
 // Eight streaming warps each take chunks warp, warp + 8, ... of the row,
 // copied into the warp's shared-memory ring, and screen them against a bar:
-// a key at or below it cannot be among the row's k best.  A key above the
-// bar goes at once into the warp's register list of its best keys (its k-th
-// best is then a bar itself).  Every bar used is valid because at least k
-// keys of the row lie above it:
+// a key at or below it cannot be among the row's k best.  Vectors that pass
+// wait in a per-warp queue; 32 at a time become keys, those above the bar
+// are staged, and staged keys merge 32 at a time (bitonic sort, then a
+// bitonic merge) into the warp's register list of its best keys.  Every bar
+// used is valid because at least k keys of the row lie above it:
 //  - a warp's own k-th best key;
 //  - the m-th largest of the warps' published rank-r keys (r = ceil(k / 8),
 //    m = ceil(k / r)): m warps each hold r keys at or above it, m r >= k

@@ -66,10 +66,6 @@ constexpr int kMaxStages = 6;
 constexpr int kMinStages = 4;
 constexpr int kMaxConsumerWarps = 24;
 constexpr int kPublishers = 2;
-// Pass-1 subgroups: with an even number of pass-1 warps they split into this
-// many groups that take alternate units, so that one group's per-unit
-// latencies (waits, reductions, hand-off) overlap another group's loop.
-constexpr int kPass1Groups = 2;
 constexpr int kGatherers = 4;
 static_assert(kMinStages >= kGatherers && kMinStages >= kPublishers, "stage reuse order");
 constexpr int kMaxSmemOffsets = 4096; // row_offsets entries kept in shared memory
@@ -537,10 +533,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
   // pass-1 warps [0, NW1), pass-2 warps [NW1, NCW) (labels on)
   const int NW1 = NEED_CONF ? P.nw1 : NCW;
   const int NW2 = NCW - NW1;
-  const int NT2 = NW2 > 0 ? NW2 * 32 : 32;
-  // pass-1 subgroups (units i = g, g + NG1, ...), G1 warps each
-  const int NG1 = NW1 % kPass1Groups == 0 ? kPass1Groups : 1;
-  const int G1 = NW1 / NG1;
+  const int NT1 = NW1 * 32, NT2 = NW2 > 0 ? NW2 * 32 : 32;
   constexpr int W_PROD = NCW, W_PUB = NCW + 1, W_GATH = NCW + 1 + kPublishers;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   const RowsSmem sm{smem_raw, P.rowbuf};
@@ -571,8 +564,8 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
       for (int s = 0; s < NS; ++s) {
         mbar_init(sm.full(s), 3);  // bulk-copy arm, RowInfo release, cp.async completion
         // pass-1 warps (labels off) or the pass-2 group, + publisher + gatherer
-        mbar_init(sm.empty(s), (NEED_CONF ? 1 : G1) + 2);
-        mbar_init(sm.partbar(s), G1);
+        mbar_init(sm.empty(s), (NEED_CONF ? 1 : NW1) + 2);
+        mbar_init(sm.partbar(s), NW1);
         mbar_init(sm.statsbar(s), 1);
       }
       mbar_init(smem_addr(smem_raw + kOffTailBar), 1);
@@ -593,15 +586,11 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
     // Labels on: warps [0, NW1) run pass 1, warps [NW1, NCW) pass 2, each
     // group on its own stream of units.  Labels off: all run pass 1.
     if (warp < NW1) {
-      const int g1 = warp / G1;  // this warp's subgroup
-      const int ct = tid - g1 * G1 * 32, st1 = G1 * 32;
+      const int ct = tid;
       RingPos rp{0, 0u};
-      for (int w = 0; w < g1; ++w) rp.next(NS);
-      for (int32_t i = g1; i < n_units; i += NG1) {  // pass 1 of unit i
+      for (int32_t i = 0; i < n_units; ++i, rp.next(NS)) {  // pass 1 of unit i
         const int s = rp.idx;
-        const uint32_t par = rp.par;
-        for (int w = 0; w < NG1; ++w) rp.next(NS);
-        mbar_wait(sm.full(s), par, timeout);
+        mbar_wait(sm.full(s), rp.par, timeout);
         const RowInfo info = *sm.info(s);
         bool bad = false;
         const Slice s_t = slice_t(info), s_d = slice_d(info);
@@ -609,16 +598,16 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         const bool fast = NEED_Z && info.pair && slice_aligned<ES>(s_t) &&
                           slice_aligned<ES>(s_d) &&
                           pass1_pair_fast<ES, TRACK>(sm.tbuf(s), sm.dbuf(s), s_t.nbytes >> 4, sc,
-                                                     ct, st1, a_t, a_d, s_t.v0);
+                                                     ct, NT1, a_t, a_d, s_t.v0);
         if (!fast) {  // general path: per-thread partials, then a warp merge
-          a_t = pass1_thread<ES, NEED_Z, TRACK>(sm.tbuf(s), s_t, sc, ct, st1, bad);
-          a_d = info.pair ? pass1_thread<ES, NEED_Z, TRACK>(sm.dbuf(s), s_d, sc, ct, st1, bad)
+          a_t = pass1_thread<ES, NEED_Z, TRACK>(sm.tbuf(s), s_t, sc, ct, NT1, bad);
+          a_d = info.pair ? pass1_thread<ES, NEED_Z, TRACK>(sm.dbuf(s), s_d, sc, ct, NT1, bad)
                           : rstat_empty();
           rstat_warp_reduce2<true>(a_t, a_d);
         }
         const unsigned badw = __ballot_sync(0xffffffffu, bad);
         if (lane == 0) {
-          float* w = sm.part(s, warp - g1 * G1);
+          float* w = sm.part(s, warp);
           w[R_HT] = a_t.h; w[R_ST] = a_t.s; w[R_MT] = a_t.m; w[R_IT] = __int_as_float(a_t.i);
           w[R_HD] = a_d.h; w[R_SD] = a_d.s; w[R_MD] = a_d.m; w[R_ID] = __int_as_float(a_d.i);
           w[R_BAD] = __int_as_float((badw ? SV_DEVERR_NAN : 0) | (timeout ? SV_DEVERR_TIMEOUT : 0));
@@ -627,7 +616,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
         }
       }
     } else {
-      const int ct = tid - NW1 * 32;
+      const int ct = tid - NT1;
       RingPos rp{0, 0u};
       for (int32_t j = 0; j < n_units; ++j, rp.next(NS)) {  // pass 2 of unit j, then release its stage
         const int s = rp.idx;
@@ -701,7 +690,7 @@ __global__ void __launch_bounds__(rows_threads(NCW), 1) rows_kernel(const Params
       const RowInfo info = *sm.info(s);
       RStat b_t = rstat_empty(), b_d = rstat_empty();
       int flags = 0;
-      if (lane < G1) {
+      if (lane < NW1) {
         const float* w = sm.part(s, lane);
         b_t = RStat{w[R_HT], w[R_ST], w[R_MT], __float_as_int(w[R_IT])};
         b_d = RStat{w[R_HD], w[R_SD], w[R_MD], __float_as_int(w[R_ID])};

@@ -326,9 +326,7 @@ def stages(n):
 @pytest.mark.parametrize("L", [None, 2504])
 def test_consumer_warp_splits(cuda_lib, warps, pass1, L):
     """Any split of the consumer warps between pass 1 and pass 2 gives the
-    oracle's results (labels on, so both groups run); an even number of
-    pass-1 warps runs as two subgroups taking alternate units, an odd one
-    as a single group."""
+    oracle's results (labels on, so both groups run)."""
     w = W.make_workload(W.WORKLOADS[3], W.SAMPLE, seed=23, device=DEV, B=24, V=30011)
     with tuning(warps=warps, pass1_warps=pass1), slice_len(L):
         run_and_compare(cuda_lib, w)
