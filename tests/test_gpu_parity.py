@@ -555,3 +555,18 @@ def test_small_residual_mass_is_drawn_from(cuda_lib):
     for r in range(6):
         assert int(out.accept_len[r]) == 0
         assert toks[2 * r] == int(ys[r]), (r, Rs[r], toks[2 * r], int(ys[r]))
+
+
+@pytest.mark.parametrize("V", [1, 2, 3, 7, 17])
+@pytest.mark.parametrize("idx", [0, 2])  # fp32, bf16
+def test_tiny_vocabularies(cuda_lib, idx, V):
+    """Degenerate vocabularies (a single token, rows shorter than one 16-byte
+    vector, odd lengths): unfiltered in both modes, the small kept-set path
+    and the general one."""
+    for mode in (W.SAMPLE, W.GREEDY):
+        w = W.make_workload(W.WORKLOADS[idx], mode, seed=90 + V, device=DEV, V=V, lens=[1, 3, 5, 2])
+        run_and_compare(cuda_lib, w, T=1.0, top_k=0, top_p=1.0, mode=mode)
+    w = W.make_workload(W.WORKLOADS[idx], W.SAMPLE, seed=95 + V, device=DEV, V=V, lens=[4, 1, 5])
+    run_and_compare(cuda_lib, w, T=1.0, top_k=min(2, V), top_p=0.7)  # kept sets <= 64
+    run_and_compare(cuda_lib, w, T=1.0, top_k=0, top_p=0.8)          # top-p over the vocabulary
+    run_and_compare(cuda_lib, w, T=0.7, top_k=100, top_p=1.0)        # top_k >= V: off
