@@ -570,3 +570,26 @@ def test_tiny_vocabularies(cuda_lib, idx, V):
     run_and_compare(cuda_lib, w, T=1.0, top_k=min(2, V), top_p=0.7)  # kept sets <= 64
     run_and_compare(cuda_lib, w, T=1.0, top_k=0, top_p=0.8)          # top-p over the vocabulary
     run_and_compare(cuda_lib, w, T=0.7, top_k=100, top_p=1.0)        # top_k >= V: off
+
+
+@pytest.mark.parametrize("mode", [W.SAMPLE, W.GREEDY])
+def test_maximum_request_length(cuda_lib, mode):
+    """l_r = SV_MAX_LEN (256 target rows) next to short requests: random rows
+    unfiltered and on both filtered paths, then identical target and draft
+    rows, where every drafted token is accepted and the bonus row drawn."""
+    lens = [256, 1, 200, 256]
+    w = W.make_workload(W.WORKLOADS[3], mode, seed=47, device=DEV, V=3001, lens=lens)
+    run_and_compare(cuda_lib, w, max_len=256)
+    run_and_compare(cuda_lib, w, max_len=256, top_k=20, top_p=0.9)  # kept sets <= 64
+    run_and_compare(cuda_lib, w, max_len=256, top_k=0, top_p=0.9)   # general path
+    offs = w.row_offsets.cpu().numpy()
+    t = w.target.clone()
+    d = torch.cat([t[offs[r]:offs[r + 1] - 1] for r in range(w.B)]).clone()
+    if mode == W.GREEDY:
+        x = torch.argmax(d.float(), 1)
+    else:
+        g = torch.Generator(device=DEV).manual_seed(6)
+        x = torch.multinomial(torch.softmax(d.float(), 1), 1, generator=g).flatten()
+    same = _pair_workload(t, d, x, lens, w.uniforms, mode=mode)
+    out, _ = run_and_compare(cuda_lib, same, max_len=256)
+    assert out.accept_len.cpu().tolist() == [n - 1 for n in lens]
