@@ -277,20 +277,24 @@ __device__ __forceinline__ int gbin(float y) {
 // sum(w >> s) << s <= mass < (sum(w >> s) + count) << s.
 __device__ __forceinline__ int gshift(int b) { return max(0, 28 - (b >> 3)); }
 
-// The c-th smallest id (c >= 1) among the elements with key == t: warps
-// count over contiguous ranges of the row (kGUnroll vectors a lane in
-// flight), the warp whose range holds the c-th walks it, 32 vectors a step
-// with kGUnroll steps of loads in flight.
+// The c-th smallest id (c >= 1) among the elements with key == t (all
+// threads of the CTA; tb: 16 x 256 words of shared scratch).  Warps count
+// the ties of each block of their contiguous ranges of the row (kGUnroll
+// vectors a lane in flight); warp 0 finds the block holding the c-th along
+// the id order, and the warp owning it walks just that block.
 template <int ES>
 __device__ __forceinline__ int32_t g_tie_id(const unsigned char* row, int32_t V, uint32_t t,
                                          unsigned long long c, unsigned long long* red,
-                                         int32_t* shared_id) {
+                                         int32_t* shared_id, uint32_t (*tb)[256]) {
   constexpr int VEC = 16 / ES;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int kGUnroll = g_unroll<ES>();
+  constexpr int kStep = 32 * kGUnroll;  // vectors a warp reads per round
   const GCover cv = g_cover<ES>(row, V);
   const int32_t per = (cv.nvec + kGWarps - 1) / kGWarps;  // vectors per warp range
   const int32_t k0 = min(cv.nvec, warp * per), k1 = min(cv.nvec, k0 + per);
+  // blocks of bstep vectors (a multiple of kStep), at most 256 a warp
+  const int32_t bstep = kStep * ((per + kStep * 256 - 1) / (kStep * 256));
   auto scan = [&](const uint4& w, int32_t k) {  // tie mask of vector k
     float x[VEC];
     g_unpack<ES>(w, x);
@@ -302,46 +306,74 @@ __device__ __forceinline__ int32_t g_tie_id(const unsigned char* row, int32_t V,
     }
     return m;
   };
-  unsigned long long n = 0;
-  for (int32_t kb = k0; kb < k1; kb += 32 * kGUnroll) {
+  // ---- every warp: the ties in each block of its range
+  for (int i = lane; i < 256; i += 32) tb[warp][i] = 0u;
+  __syncwarp();
+  for (int32_t kb = k0; kb < k1; kb += kStep) {
     uint4 w[kGUnroll];
 #pragma unroll
     for (int u = 0; u < kGUnroll; ++u) {
       const int32_t k = kb + 32 * u + lane;
       w[u] = k < k1 ? g_ld16(cv.base, k) : make_uint4(0u, 0u, 0u, 0u);
     }
+    unsigned n = 0;
 #pragma unroll
     for (int u = 0; u < kGUnroll; ++u) {
       const int32_t k = kb + 32 * u + lane;
       if (k < k1) n += __popc(scan(w[u], k));
     }
+    n = __reduce_add_sync(0xffffffffu, n);
+    if (lane == 0) tb[warp][(kb - k0) / bstep] += n;
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) n += __shfl_xor_sync(0xffffffffu, n, off);
-  if (lane == 0) red[warp] = n;
   if (threadIdx.x == 0) *shared_id = -1;
   __syncthreads();
-  unsigned long long before = 0;
-  int owner = -1;
-  for (int w = 0; w < kGWarps; ++w) {
-    if (owner < 0 && before + red[w] >= c) owner = w;
-    if (owner < 0) before += red[w];
+  // ---- warp 0: the block holding the c-th tie along the id order (warp
+  //      ranges in order, blocks in order inside each); lane l sums entries
+  //      128 l .. 128 l + 127 of the flattened [warp][block] table
+  if (warp == 0) {
+    const uint32_t* flat = &tb[0][0];
+    unsigned long long ls = 0;
+    for (int i = 0; i < 128; ++i) ls += flat[128 * lane + i];
+    unsigned long long incl = ls;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const unsigned hit = __ballot_sync(0xffffffffu, incl >= c && incl - ls < c);
+    if (hit && lane == __ffs(hit) - 1) {
+      unsigned long long before = incl - ls;
+      int e = 128 * lane;
+      while (before + flat[e] < c) before += flat[e++];
+      red[0] = static_cast<unsigned long long>(e);
+      red[1] = c - before;  // the tie's rank inside that block, >= 1
+    }
+    if (!hit && lane == 0) {  // fewer than c ties (no such row): no id
+      red[0] = ~0ull;
+      red[1] = 0ull;
+    }
   }
-  if (warp == owner) {
-    unsigned long long left = c - before;  // >= 1
+  __syncthreads();
+  const unsigned long long eb = red[0];
+  unsigned long long left = red[1];
+  __syncthreads();
+  if (eb != ~0ull && warp == static_cast<int>(eb >> 8)) {
+    // ---- the owner warp walks that one block
+    const int32_t bk0 = k0 + static_cast<int32_t>(eb & 255u) * bstep;
+    const int32_t bk1 = min(k1, bk0 + bstep);
     bool found = false;
-    for (int32_t kb = k0; kb < k1 && !found; kb += 32 * kGUnroll) {
+    for (int32_t kb = bk0; kb < bk1 && !found; kb += kStep) {
       uint4 w[kGUnroll];
 #pragma unroll
       for (int u = 0; u < kGUnroll; ++u) {
         const int32_t k = kb + 32 * u + lane;
-        w[u] = k < k1 ? g_ld16(cv.base, k) : make_uint4(0u, 0u, 0u, 0u);
+        w[u] = k < bk1 ? g_ld16(cv.base, k) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int u = 0; u < kGUnroll; ++u) {
         if (found) break;
         const int32_t k = kb + 32 * u + lane;
-        const unsigned m = k < k1 ? scan(w[u], k) : 0u;
+        const unsigned m = k < bk1 ? scan(w[u], k) : 0u;
         unsigned cnt = __popc(m), incl = cnt;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -486,7 +518,7 @@ __device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, fl
   // keys, and when it spans at most 256 keys one level with digit key - klo
   // replaces the two byte levels.  Digits are taken of key - base (base klo
   // for the one level, else 0; keys below base wrap and match no prefix).
-  uint32_t klo = 0;
+  uint32_t klo = 0, khi = 0;
   bool single = false;
   if (ES == 2) {
     auto G = [&](uint32_t k) { return gbin(fmaf(gkey_value<ES>(k), sc, -h)); };
@@ -503,6 +535,7 @@ __device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, fl
       if (G(mid) >= ba) lo = mid; else hi = mid - 1;
     }
     single = lo >= klo && lo - klo < 256u;
+    khi = lo;
   }
   const uint32_t base = single ? klo : 0u;
   uint32_t prefix = 0;
@@ -518,6 +551,19 @@ __device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, fl
     // first, the warp-aggregated updates only when some lane of the warp
     // holds a logit of the run
     unsigned long long mb = 0;  // the thread's share of the mass before the run
+    if (ES == 2 && single) {
+      // one level over a bf16 run of at most 256 keys [klo, khi]: the bins
+      // never rise along the key order, so membership is a key comparison;
+      // every element of a key has the same value and weight, so only the
+      // count of each digit (key - klo) is kept, and its mass is count x
+      // weight below
+      g_for_row<ES>(row, V, [&](int32_t, float x, bool ok) {
+        if (!ok) return;
+        const uint32_t key = gkey<ES>(x);
+        if (key > khi) mb += gweight(x, sc, h);
+        else if (key >= klo) atomicAdd(&hist->dn[warp][key - klo], 1u);
+      });
+    } else
     for (int32_t k0 = tid - lane; k0 < cv.nvec; k0 += kGUnroll * kGThreads) {
       uint4 wv[kGUnroll];
 #pragma unroll
@@ -551,7 +597,17 @@ __device__ __forceinline__ GSel g_digits(const unsigned char* row, int32_t V, fl
       }
     }
     __syncthreads();
-    {  // the warps' histograms summed into warp 0's: counts by threads 0..255,
+    if (ES == 2 && single) {  // counts summed; a digit's mass is its count x its key's weight
+      if (tid < 256) {
+        uint32_t c = 0;
+#pragma unroll
+        for (int q = 0; q < kGWarps; ++q) c += hist->dn[q][tid];
+        hist->dn[0][tid] = c;
+        hist->dm[0][tid] = c ? static_cast<unsigned long long>(c) *
+                                   gweight(gkey_value<ES>(klo + tid), sc, h)
+                             : 0ull;
+      }
+    } else {  // the warps' histograms summed into warp 0's: counts by threads 0..255,
        // masses by threads 256..511, one bin each
       const int j = tid & 255;
       if (tid < 256) {
@@ -699,7 +755,7 @@ __device__ __forceinline__ GRow g_select_row(const Params& P, const unsigned cha
     const unsigned long long wt = gweight(gkey_value<ES>(s.t), sc, h);
     zk = s.m_before + s.m_above + ck * wt;
     g.thr_key = s.t;
-    if (!use_p) g.thr_id = g_tie_id<ES>(row, V, s.t, ck, red, sid);
+    if (!use_p) g.thr_id = g_tie_id<ES>(row, V, s.t, ck, red, sid, hist->dn);
   }
   if (use_p) {
     // ---- top-p: the shortest prefix of the order whose mass reaches top_p *
@@ -730,7 +786,7 @@ __device__ __forceinline__ GRow g_select_row(const Params& P, const unsigned cha
     unsigned long long cp = wt > 0 ? (target - m_above + wt - 1) / wt : s.ties;
     cp = max(1ull, min(cp, s.ties));
     g.thr_key = s.t;
-    g.thr_id = g_tie_id<ES>(row, V, s.t, cp, red, sid);
+    g.thr_id = g_tie_id<ES>(row, V, s.t, cp, red, sid, hist->dn);
     zk = m_above + cp * wt;
   }
   g.z = static_cast<float>(static_cast<double>(zk) / static_cast<double>(kGFix));
