@@ -264,3 +264,106 @@ def spec_verify_schedule(conf: torch.Tensor, sps: torch.Tensor, *, out_lens=None
         raise SpecVerifyError(rc)
     return out_lens, out_theta
 
+
+
+# ---- the verify step over a vocabulary split across ranks
+#      (include/spec_verify_shard.h)
+
+SV_SHARD_MAX_WORLD = 32
+SV_SHARD_REC_WORDS, SV_SHARD_ROW_WORDS, SV_SHARD_MASS_WORDS = 12, 8, 4
+_lib.spec_verify_shard_stats.argtypes = [_vp, _vp, _i32, _i32, _i32, _vp, _vp, _vp,
+                                         _i32, _i32, _i32, _i32, _f32, _vp, _vp]
+_lib.spec_verify_shard_merge.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32,
+                                         _f32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.spec_verify_shard_masses.argtypes = [_vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                          _i32, _f32, _i32, _vp, _vp]
+_lib.spec_verify_shard_draw.argtypes = [_vp, _i32, _i32, _vp, _vp, _i32, _i32, _vp, _vp, _vp,
+                                        _vp, _vp, _i32, _i32, _i32, _i32, _f32, _i32, _vp, _vp,
+                                        _vp, _vp]
+_lib.spec_verify_shard_finish.argtypes = [_vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _vp,
+                                          _vp]
+for _name in ("spec_verify_shard_stats", "spec_verify_shard_merge", "spec_verify_shard_masses",
+              "spec_verify_shard_draw", "spec_verify_shard_finish"):
+    getattr(_lib, _name).restype = ctypes.c_int
+
+
+def _check(rc):
+    if rc != SV_OK:
+        raise SpecVerifyError(rc)
+
+
+def _stream_of(t, stream):
+    s = torch.cuda.current_stream(t.device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def spec_verify_shard_stats(target_shard, draft_shard, v_begin, V, draft_tokens, verify_lens,
+                            row_offsets, *, max_len, temperature, out_rec, stream=None):
+    """Step 1 on this rank: partial statistics of its columns (target_shard
+    [N_t, V_q], draft_shard [N_d, V_q], ids v_begin .. v_begin + V_q - 1 of
+    a vocabulary of V) into out_rec [N_t, 12] int32."""
+    n_t, vq = target_shard.shape
+    with torch.cuda.device(target_shard.device):
+        _check(_lib.spec_verify_shard_stats(
+            _ptr(target_shard), _ptr(draft_shard) if draft_shard.numel() else None, _i32(vq),
+            _i32(v_begin), _i32(V), _ptr(draft_tokens) if draft_tokens.numel() else None,
+            _ptr(verify_lens), _ptr(row_offsets), _i32(verify_lens.numel()), _i32(n_t),
+            _i32(max_len), _i32(_dtype_code(target_shard)), _f32(temperature), _ptr(out_rec),
+            _stream_of(target_shard, stream)))
+
+
+def spec_verify_shard_merge(recs, draft_tokens, uniforms, verify_lens, row_offsets, V, *,
+                            max_len, temperature, mode, out_merged, out: Outputs, stream=None):
+    """Step 1 on every rank: merge the gathered records recs [world, N_t, 12]."""
+    world, n_t, _ = recs.shape
+    with torch.cuda.device(recs.device):
+        _check(_lib.spec_verify_shard_merge(
+            _ptr(recs), _i32(world), _ptr(draft_tokens) if draft_tokens.numel() else None,
+            _ptr(uniforms), _ptr(verify_lens), _ptr(row_offsets), _i32(verify_lens.numel()),
+            _i32(V), _i32(n_t), _i32(max_len), _f32(temperature), _i32(mode), _ptr(out_merged),
+            _ptr(out.tokens), _ptr(out.accept_len), _ptr(out.row_stats), _ptr(out.dev_error),
+            _stream_of(recs, stream)))
+
+
+def spec_verify_shard_masses(target_shard, draft_shard, merged, verify_lens, row_offsets,
+                             accept_len, *, max_len, temperature, all_rows, out_mass,
+                             stream=None):
+    """Step 2 on this rank: its shares of the masses into out_mass [N_t, 4]."""
+    n_t, vq = target_shard.shape
+    with torch.cuda.device(target_shard.device):
+        _check(_lib.spec_verify_shard_masses(
+            _ptr(target_shard), _ptr(draft_shard) if draft_shard.numel() else None, _i32(vq),
+            _ptr(merged), _ptr(verify_lens), _ptr(row_offsets), _ptr(accept_len),
+            _i32(verify_lens.numel()), _i32(n_t), _i32(max_len), _i32(_dtype_code(target_shard)),
+            _f32(temperature), _i32(1 if all_rows else 0), _ptr(out_mass),
+            _stream_of(target_shard, stream)))
+
+
+def spec_verify_shard_draw(masses, rank, target_shard, draft_shard, v_begin, merged, uniforms,
+                           verify_lens, row_offsets, *, max_len, temperature, mode,
+                           out: Outputs, out_cand, stream=None):
+    """Step 3 on every rank: labels into out.conf and, sampling, this rank's
+    candidate token per request into out_cand [B] (-1 where another rank
+    owns the draw)."""
+    world = masses.shape[0]
+    n_t, vq = target_shard.shape
+    with torch.cuda.device(target_shard.device):
+        _check(_lib.spec_verify_shard_draw(
+            _ptr(masses), _i32(world), _i32(rank), _ptr(target_shard),
+            _ptr(draft_shard) if draft_shard.numel() else None, _i32(vq), _i32(v_begin),
+            _ptr(merged), _ptr(uniforms), _ptr(verify_lens), _ptr(row_offsets),
+            _ptr(out.accept_len), _i32(verify_lens.numel()), _i32(n_t), _i32(max_len),
+            _i32(_dtype_code(target_shard)), _f32(temperature), _i32(mode), _ptr(out.conf),
+            _ptr(out_cand), _ptr(out.dev_error), _stream_of(target_shard, stream)))
+
+
+def spec_verify_shard_finish(cands, merged, verify_lens, row_offsets, *, out: Outputs,
+                             stream=None):
+    """Step 3 on every rank: the final tokens from the gathered candidates
+    cands [world, B]."""
+    world, B = cands.shape
+    with torch.cuda.device(cands.device):
+        _check(_lib.spec_verify_shard_finish(
+            _ptr(cands), _i32(world), _ptr(merged), _ptr(verify_lens), _ptr(row_offsets),
+            _ptr(out.accept_len), _i32(B), _i32(out.tokens.numel()), _ptr(out.tokens),
+            _ptr(out.dev_error), _stream_of(cands, stream)))

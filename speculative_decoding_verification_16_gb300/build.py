@@ -1,7 +1,7 @@
 """Build step of the C-ABI library ``libspecverify.so`` (sm_103a).
 
-One translation unit, one ``-gencode``, compiled in-tree next to this file
-with ``nvcc -shared``.  Rebuilds only when a source or the header is newer
+Two translation units (the verify step, and its vocabulary-sharded form),
+one ``-gencode``, compiled in-tree next to this file with ``nvcc -shared``.  Rebuilds only when a source or the header is newer
 than the library.
 """
 
@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = [os.path.join(CSRC, "spec_verify.cu")]
+SOURCES = [os.path.join(CSRC, "spec_verify.cu"), os.path.join(CSRC, "sv_shard.cu")]
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 
