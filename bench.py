@@ -34,6 +34,14 @@ sample of requests (near ties, open accept chains, mismatches).
 confidences are the verify step's own labels on the ragged workload; the
 SPS curve is synthetic: flat to 1,024 tokens, then falling as 1/B), with the
 fp64 oracle timed beside it.
+
+--component split prints one line for the vocabulary-split verify
+(include/spec_verify_shard.h) on the same workload: the columns of every row
+split over --split-world ranks whose steps run in lockstep on this one GPU
+(the all-gathers are stacks in rank order), each phase timed with CUDA
+events and divided by the number of ranks to give one rank's time, L2
+flushed before both passes over the logits (the statistics pass and the
+masses pass).
 """
 
 import os
@@ -77,7 +85,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true",
                     help="skip the per-workload lines (all five workloads in their modes)")
-    ap.add_argument("--component", choices=("verify", "schedule"), default="verify")
+    ap.add_argument("--component", choices=("verify", "schedule", "split"), default="verify")
+    ap.add_argument("--split-world", type=int, default=8,
+                    help="--component split: ranks the vocabulary is split over")
     ap.add_argument("--top-k", type=int, default=None, help="override the workload's top_k")
     ap.add_argument("--top-p", type=float, default=None, help="override the workload's top_p")
     return ap.parse_args()
@@ -681,11 +691,110 @@ def run_schedule(args, rank):
         }), flush=True)
 
 
+def run_split(args, rank):
+    """Vocabulary-split verify: one rank's kernel times, emulated in lockstep."""
+    from speculative_decoding_verification_16_gb300.sharded import ShardRank, split_columns
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    spec = W.WORKLOADS[args.workload]
+    mode = W.SAMPLE if args.mode == "sample" else W.GREEDY
+    w = W.make_workload(spec, mode, seed=args.workload, device=dev)
+    n_t, V = w.target.shape
+    n_d = w.draft.shape[0]
+    world = args.split_world
+    ranks = [ShardRank(q, world, v0, V, w.target[:, v0:v0 + vq].contiguous(),
+                       w.draft[:, v0:v0 + vq].contiguous(), w.draft_tokens, w.uniforms,
+                       w.verify_lens, w.row_offsets, max_len=spec.max_len,
+                       temperature=spec.temperature, mode=mode, want_conf=True)
+             for q, (v0, vq) in enumerate(split_columns(V, world))]
+    sample = mode == W.SAMPLE
+    flush = torch.zeros(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    names = ["stats", "gather 1", "merge", "masses", "gather 2", "draw", "gather 3", "finish"]
+
+    def step(ev):
+        # ev: events before each phase and one after the last (or None)
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        flush.add_(1)
+        mark(0)
+        for r in ranks:
+            r.stats()
+        mark(1)
+        recs = torch.stack([r.rec for r in ranks])
+        mark(2)
+        for r in ranks:
+            r.merge(recs)
+        if ev is not None:
+            ev[3].record(stream)
+        flush.add_(1)  # the masses pass re-reads the columns from HBM
+        mark(4)
+        for r in ranks:
+            r.masses()
+        mark(5)
+        masses = torch.stack([r.mass for r in ranks])
+        mark(6)
+        for r in ranks:
+            r.draw(masses)
+        mark(7)
+        if sample:
+            cands = torch.stack([r.cand for r in ranks])
+            mark(8)
+            for r in ranks:
+                r.finish(cands)
+        else:
+            mark(8)
+        mark(9)
+
+    for _ in range(max(3, args.warmup)):
+        step(None)
+    torch.cuda.synchronize()
+    K = min(args.steps, 200)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(K)]
+    for k in range(K):
+        step(evs[k])
+    torch.cuda.synchronize()
+    # phase ms per step; [3] -> [4] is the flush, not a phase
+    spans = [(0, 1), (1, 2), (2, 3), (4, 5), (5, 6), (6, 7), (7, 8), (8, 9)]
+    ph = {n: statistics.mean(e[a].elapsed_time(e[b]) for e in evs) for n, (a, b) in zip(names, spans)}
+    per_rank = {n: ph[n] / world for n in names if not n.startswith("gather")}
+    rank_ms = sum(per_rank.values())
+    es = w.target.element_size()
+    vq_max = max(vq for _, vq in split_columns(V, world))
+    rank_bytes = (n_t + n_d) * vq_max * es  # one pass over the widest rank's columns
+    top = max(("stats", "masses"), key=lambda n: per_rank[n])
+    peak, src = hbm_peak()
+    ach = rank_bytes / (per_rank[top] * 1e-3) / 1e9
+    if rank == 0:
+        print(json.dumps({
+            "metric": "vocabulary-split verify: drafted positions/s of one rank's kernels",
+            "value": n_d / (rank_ms * 1e-3), "unit": UNIT, "n_gpus": 1, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": rank_ms, "higher_is_better": True,
+            "scaling": "strong", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": spec.name, "world": world, "mode": args.mode,
+                       "labels": True,
+                       "ranks": "emulated in lockstep on one GPU; each phase's time / world",
+                       "l2": "flushed before the stats pass and before the masses pass"},
+            "phases_us_per_rank": {n: 1e3 * v for n, v in per_rank.items()},
+            "gather_us_all_ranks": {n: 1e3 * ph[n] for n in names if n.startswith("gather")},
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+                         "frac": ach / peak, "traffic": None, "kernel": f"shard_{top}_kernel",
+                         "bytes_per_launch": rank_bytes,
+                         "mean_launch_ms": per_rank[top], "peak_source": src},
+            "gpu_launches": K * world * (5 if sample else 4),
+        }), flush=True)
+
+
 def main():
     args = parse()
     world, rank, local = dist_setup()
     if args.component == "schedule":
         run_schedule(args, rank)
+    elif args.component == "split":
+        run_split(args, rank)
     elif args.impl == "reference":
         run_reference(args, world, rank)
     else:
