@@ -50,6 +50,22 @@ class ShardRank:
         for t in (target_shard, draft_shard, draft_tokens, uniforms, verify_lens, row_offsets):
             if not t.is_contiguous():
                 raise ValueError("inputs must be contiguous")
+        if target_shard.dim() != 2 or draft_shard.dim() != 2:
+            raise ValueError("shard logits must be [rows, V_q]")
+        vq = target_shard.shape[1]
+        if draft_shard.dtype != target_shard.dtype or \
+                (draft_shard.shape[0] and draft_shard.shape[1] != vq):
+            raise ValueError("draft columns must match the target columns (dtype and V_q)")
+        if not (0 <= v_begin and v_begin + vq <= V):
+            raise ValueError(f"columns [{v_begin}, {v_begin + vq}) outside [0, {V})")
+        if not 0 <= rank < world:
+            raise ValueError(f"rank {rank} outside a world of {world}")
+        for name, t, dt in (("draft_tokens", draft_tokens, torch.int32),
+                            ("uniforms", uniforms, torch.float32),
+                            ("verify_lens", verify_lens, torch.int32),
+                            ("row_offsets", row_offsets, torch.int32)):
+            if t.dtype != dt:
+                raise TypeError(f"{name} must be {dt}, got {t.dtype}")
         self.rank, self.world, self.v_begin, self.V = rank, world, v_begin, V
         self.tgt, self.drf = target_shard, draft_shard
         self.draft_tokens, self.uniforms = draft_tokens, uniforms

@@ -232,3 +232,37 @@ def test_protocol_over_gloo_ranks(world):
     for rank in range(world):
         for (sample, want_conf), log in zip(MODES, got[rank]):
             assert log == expected_log(world, sample, want_conf)
+
+
+def test_shard_rank_rejects_inconsistent_inputs():
+    """ShardRank checks shapes, dtypes and the column range on the host
+    before any call reaches the library."""
+    from speculative_decoding_verification_16_gb300.sharded import ShardRank
+    B, n_t, vq = 2, 6, 10
+    ok = dict(target_shard=torch.zeros((n_t, vq), dtype=torch.bfloat16),
+              draft_shard=torch.zeros((n_t - B, vq), dtype=torch.bfloat16),
+              draft_tokens=torch.zeros(n_t - B, dtype=torch.int32),
+              uniforms=torch.zeros(n_t, dtype=torch.float32),
+              verify_lens=torch.tensor([3, 3], dtype=torch.int32),
+              row_offsets=torch.tensor([0, 3, 6], dtype=torch.int32))
+
+    def make(rank=0, world=2, v_begin=0, V=20, **over):
+        kw = dict(ok)
+        kw.update(over)
+        return ShardRank(rank, world, v_begin, V, **kw)
+
+    make()  # consistent: accepted
+    with pytest.raises(ValueError):
+        make(draft_shard=torch.zeros((n_t - B, vq), dtype=torch.float32))
+    with pytest.raises(ValueError):
+        make(draft_shard=torch.zeros((n_t - B, vq + 1), dtype=torch.bfloat16))
+    with pytest.raises(ValueError):
+        make(v_begin=15)                       # columns 15..24 of a vocabulary of 20
+    with pytest.raises(ValueError):
+        make(rank=2)
+    with pytest.raises(ValueError):
+        make(target_shard=torch.zeros((vq, n_t), dtype=torch.bfloat16).t())  # not contiguous
+    with pytest.raises(TypeError):
+        make(draft_tokens=torch.zeros(n_t - B, dtype=torch.int64))
+    with pytest.raises(TypeError):
+        make(uniforms=torch.zeros(n_t, dtype=torch.float64))
